@@ -1,0 +1,109 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of ``oracle/oracle.c`` (a dropped
+term, a wrong sign, index or operand), builds it with gcc on the CPU, and runs
+every pin in ``test_oracle_pins.py`` against it: at least one pin must fail.
+The oracle itself is never modified.
+"""
+import inspect
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "relu_dropped": ("double r = x[h] > 0.0 ? x[h] : 0.0;", "double r = x[h];"),
+    "relu_after_sum": ("J->out[row * J->out_stride + p] = s * acc;",
+                       "J->out[row * J->out_stride + p] = s * (acc > 0.0 ? acc : 0.0);"),
+    "scale_dropped": ("J->out[row * J->out_stride + p] = s * acc;",
+                      "J->out[row * J->out_stride + p] = acc;"),
+    "scale_wrong_index": ("ORC_BLOCK_KEY_BYTES + 4 * (p % ORC_BLOCK_KEYS)",
+                          "ORC_BLOCK_KEY_BYTES + 4 * (p / ORC_BLOCK_KEYS)"),
+    "weight_sign_lost": ("acc += (double)w[h] * r;", "acc += fabs((double)w[h]) * r;"),
+    "key_transposed": ("J->e4m3[qrow[h * ORC_HEAD_DIM + d]] * J->e4m3[k[d]]",
+                       "J->e4m3[qrow[h * ORC_HEAD_DIM + d]] * J->e4m3[blk[d * ORC_BLOCK_KEYS + p % ORC_BLOCK_KEYS]]"),
+    "q_transposed": ("qrow[h * ORC_HEAD_DIM + d]", "qrow[d * H / 2 + h]"),
+    "slot_ignored": ("const int64_t row = (int64_t)b * n + t;\n        const uint8_t* qrow = J->q + row * H * ORC_HEAD_DIM;",
+                     "const int64_t row = (int64_t)b * n + t;\n        const uint8_t* qrow = J->q + (int64_t)b * n * H * ORC_HEAD_DIM;"),
+    "block_table_row_ignored": ("J->block_table[(int64_t)b * J->bt_stride + p / ORC_BLOCK_KEYS]",
+                                "J->block_table[p / ORC_BLOCK_KEYS]"),
+    "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "e4m3_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "bf16_page_stride_fixed": ("page * J->page_stride_bytes", "page * 16384"),
+    "bf16_group_rows": ("for (int r = g * G; r < (g + 1) * G; ++r)", "for (int r = g; r < g + G; ++r)"),
+    "bf16_key_stride": ("(int64_t)(k % ORC_BLOCK_KEYS) * ORC_HEAD_DIM * 2", "(int64_t)(k % ORC_BLOCK_KEYS) * ORC_HEAD_DIM"),
+    "schedule_ceil_split": ("int64_t base = total / num_ctas, extra = total % num_ctas;",
+                            "int64_t base = (total + num_ctas - 1) / num_ctas, extra = 0;"),
+    "schedule_skips_empty_wrong": ("if (start < prefix + nb) break;", "if (start <= prefix + nb) break;"),
+}
+
+
+def _pin_functions():
+    out = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        marks = getattr(fn, "pytestmark", [])
+        params = [m for m in marks if m.name == "parametrize"]
+        if params:
+            argnames = [a.strip() for a in params[0].args[0].split(",")]
+            for vals in params[0].args[1]:
+                vals = vals if isinstance(vals, tuple) else (vals,)
+                out.append((name, fn, dict(zip(argnames, vals))))
+        else:
+            out.append((name, fn, {}))
+    return out
+
+
+def _build_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique in oracle.c"
+    path_c = os.path.join(tmp_path, f"{name}.c")
+    path_so = os.path.join(tmp_path, f"lib{name}.so")
+    with open(path_c, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", path_c, "-o",
+                    path_so, "-lm"], check=True)
+    return path_so
+
+
+def test_every_mutant_fails_a_pin(tmp_path):
+    names = sorted(MUTANTS)
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        libs = dict(zip(names, ex.map(lambda n: _build_mutant(n, str(tmp_path)), names)))
+    golden = os.path.join(os.path.dirname(pins.__file__), "golden")
+    survivors = []
+    for name in names:
+        caught = []
+        with oracle.using_library(libs[name]):
+            for tname, fn, kwargs in _pin_functions():
+                args = dict(kwargs)
+                if "tmp_path" in inspect.signature(fn).parameters:
+                    args["tmp_path"] = tmp_path
+                if "golden_dir" in inspect.signature(fn).parameters:
+                    args["golden_dir"] = golden
+                try:
+                    fn(**args)
+                except (AssertionError, ValueError, IndexError):
+                    caught.append(tname)
+                    break
+        if not caught:
+            survivors.append(name)
+    assert not survivors, f"no pin caught: {survivors}"
+
+
+def test_unmutated_copy_passes_all_pins(tmp_path):
+    """Control: the same harness with the real source must pass every pin."""
+    path_so = os.path.join(str(tmp_path), "libcontrol.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", SRC, "-o",
+                    path_so, "-lm"], check=True)
+    with oracle.using_library(path_so):
+        for tname, fn, kwargs in _pin_functions():
+            fn(**kwargs)
