@@ -1,0 +1,167 @@
+/*
+ * pml -- paged MQA logits for the sparse-attention indexer, on GB300 (sm_103a).
+ *
+ * C ABI of libpml.so.  All tensor arguments are DEVICE pointers owned by the
+ * caller; the library never allocates, frees or synchronises, and enqueues all
+ * work on `stream` (a cudaStream_t passed as void*; NULL is the legacy default
+ * stream).  Every entry point is one or two kernel launches with no host
+ * round-trip, so it can be captured in a CUDA graph.
+ *
+ * Return value: PML_OK (0) or one of the PML_ERR_* codes.  Only conditions the
+ * host can see are reported synchronously (null or misaligned pointers, shapes
+ * outside the supported set, a CUDA launch error); nothing is launched when a
+ * check fails.  Problems only the device can see -- a block-table entry outside
+ * the cache, a bounded wait that ran out -- set bits of a sticky per-device
+ * status word (pml_device_status) and the offending access is skipped.
+ *
+ * Sources: FlashInfer documentation pages "flashinfer.attn_scores" (the
+ * definition, the output contract, "Scheduling and Setup") and
+ * "flashinfer.sdsa.indexer_scores" (the single-head case and its arguments).
+ */
+#ifndef PML_H
+#define PML_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    PML_OK = 0,
+    PML_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent sizes */
+    PML_ERR_UNSUPPORTED = 2,  /* next_n, num_heads or group size outside the supported set */
+    PML_ERR_ALIGNMENT = 3,    /* a pointer or stride not aligned as stated below */
+    PML_ERR_CUDA = 4          /* a CUDA call failed; see pml_last_cuda_error() */
+};
+
+/* Device status bits (see pml_device_status). */
+#define PML_STATUS_WAIT_TIMEOUT 1u  /* an in-kernel wait exceeded its limit; that CTA stopped early */
+#define PML_STATUS_BAD_BLOCK 2u     /* a block_table entry was outside [0, num_blocks) */
+#define PML_STATUS_BAD_REQUEST 4u   /* a group's request was outside [0, num_requests) */
+
+/* Version of this ABI (major*100 + minor). */
+int pml_version(void);
+
+/* Static description of an error code. */
+const char* pml_error_string(int code);
+
+/* The cudaError_t of the last PML_ERR_CUDA returned on this host thread. */
+int pml_last_cuda_error(void);
+
+/* Default persistent grid size for `device`: its SM count (0 on error). */
+int pml_default_num_ctas(int device);
+
+/* Number of int32 elements of a schedule for `num_ctas` CTAs: (num_ctas+1)*2. */
+int pml_schedule_meta_elems(int num_ctas);
+
+/* Block-table width that covers `max_seq_len` keys: ceil(max_seq_len / 64).
+ * ("flashinfer.attn_scores", "Scheduling and Setup": min_block_table_width.) */
+int pml_min_block_table_width(int max_seq_len);
+
+/* `max_seq_len` rounded up to whole 64-key blocks.  (Same section:
+ * padded_seq_len.) */
+int pml_padded_seq_len(int max_seq_len);
+
+/*
+ * pml_schedule -- the persistent CTA work assignment
+ * ("flashinfer.attn_scores", "Scheduling and Setup").
+ *
+ * Request b owns ceil(seq_lens[b]/64) blocks of 64 keys (none if
+ * seq_lens[b] <= 0).  All blocks, in request order, are cut into num_ctas
+ * contiguous ranges whose sizes differ by at most one, the first
+ * (total mod num_ctas) one block longer.  schedule_meta (device, int32
+ * [num_ctas+1][2], written) receives for each range the (request,
+ * block-within-request) where it starts; a start at the end and the closing
+ * entry are (batch, 0).
+ *
+ * The schedule depends on seq_lens and num_ctas only (next_n is accepted for
+ * the pages' signature and must be 1..4).  A schedule is valid only while the
+ * contents of seq_lens are unchanged: recompute it whenever they change,
+ * including on every graph replay in which they change.
+ */
+int pml_schedule(const int32_t* seq_lens, int batch, int next_n, int num_ctas,
+                 int32_t* schedule_meta, void* stream);
+
+/*
+ * pml_fp8_paged_mqa_logits ("flashinfer.attn_scores": math block, the two
+ * bullets under it, the note on the output contract).
+ *
+ *   out[b*next_n + t, p] = s_p * sum_h weights[b*next_n + t, h]
+ *                                     * relu( q[b*next_n + t, h, :] . k_p )
+ *
+ * for every request b with seq_lens[b] > 0, slot t < next_n and position
+ * p < min(seq_lens[b], max_context); the rectifier acts per head, before the
+ * weighted sum, and weights may be negative.  Key p of request b is row p%64
+ * of physical block block_table[b*bt_stride + p/64]; s_p is that row's scale.
+ * Row b*next_n+t is meaningful only for p <= seq_lens[b] - next_n + t; later
+ * positions below seq_lens[b] are written but carry no meaning (callers mask).
+ * Nothing else in `out` is written: not positions >= seq_lens[b], and not the
+ * rows of requests with seq_lens[b] == 0 (pre-fill `out` to read them).
+ *
+ * q            e4m3 [batch*next_n, num_heads, 128], contiguous, 16-byte aligned
+ * kv_fused     [num_blocks][8448] bytes, 16-byte aligned: per block 64 keys x
+ *              128 e4m3 (row-major, 8192 B), then 64 little-endian fp32
+ *              per-token scales (256 B)
+ * weights      fp32 [batch*next_n, num_heads], contiguous, 16-byte aligned
+ * seq_lens     int32 [batch]; contents are trusted (not checked)
+ * block_table  int32 [batch, bt_stride]; entries below ceil(min(seq_lens[b],
+ *              max_context)/64) must be in [0, num_blocks) (others are never
+ *              read); an entry outside is replaced by 0 and flagged
+ *              PML_STATUS_BAD_BLOCK
+ * schedule_meta  NULL (each CTA computes its range on the GPU) or the output
+ *              of pml_schedule for the same seq_lens and num_ctas
+ * num_ctas     persistent grid size; 0 = pml_default_num_ctas (only allowed
+ *              with schedule_meta == NULL)
+ * out          fp32 [batch*next_n, out_stride], 4-byte aligned;
+ *              out_stride >= max_context
+ * max_context  >= 1, and ceil(max_context/64) <= bt_stride
+ * next_n       1..4;  num_heads  8, 16, 32 or 64 (head dim fixed at 128)
+ */
+int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
+                             const float* weights, const int32_t* seq_lens,
+                             const int32_t* block_table, int64_t bt_stride,
+                             const int32_t* schedule_meta, int num_ctas, float* out,
+                             int64_t out_stride, int max_context, int batch, int next_n,
+                             int num_heads, void* stream);
+
+/*
+ * pml_indexer_scores_bf16 ("flashinfer.sdsa.indexer_scores": body and the
+ * query, key_cache, block_table, context_lengths, requests and scores
+ * parameters).
+ *
+ *   scores[r, k] = query[r, :] . key_k      (one head: no weight, no ReLU)
+ *
+ * Query rows come in `groups` uniform groups of G = rows/groups consecutive
+ * rows (1 <= G <= 8); group g owns rows [g*G, (g+1)*G), has
+ * context_lengths[g] keys and reads the pages of block-table row
+ * requests[g].  For k < min(context_lengths[g], max_context) the score is
+ * written; later entries are not written, and a group of length <= 0 reads
+ * nothing (its requests entry may hold any value).
+ *
+ * query          bf16 [rows, 128], contiguous, 16-byte aligned
+ * key_cache      page P starts at byte P*page_stride_bytes and holds 64 keys x
+ *                128 bf16 (row-major); base 16-byte aligned;
+ *                page_stride_bytes a multiple of 16 and >= 16384
+ * block_table    int32 [num_requests, bt_stride]; read entries must be in
+ *                [0, num_pages) (else replaced by 0, PML_STATUS_BAD_BLOCK)
+ * requests       int32 [groups]; read entries must be in [0, num_requests)
+ *                (else replaced by 0, PML_STATUS_BAD_REQUEST)
+ * scores         fp32 [rows, scores_stride], scores_stride >= max_context
+ * max_context    >= 1, and ceil(max_context/64) <= bt_stride
+ */
+int pml_indexer_scores_bf16(const uint16_t* query, int rows, const uint16_t* key_cache,
+                            int64_t page_stride_bytes, int64_t num_pages,
+                            const int32_t* block_table, int64_t bt_stride, int num_requests,
+                            const int32_t* context_lengths, const int32_t* requests, int groups,
+                            float* scores, int64_t scores_stride, int max_context, void* stream);
+
+/* Read (and, if clear != 0, reset) the current device's sticky status word.
+ * Synchronises with the device (waits for all work queued so far). */
+int pml_device_status(unsigned int* status, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PML_H */

@@ -1,0 +1,60 @@
+// Host-side launch records for the kernels of the paged MQA-logits library.
+// Internal to the library: the public C ABI is include/pml.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pml {
+
+struct Fp8Args {
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    const int32_t* schedule_meta;  // nullptr: computed by each CTA
+    const float* weights;
+    const uint8_t* kv_fused;
+    float* out;
+    unsigned int* status;
+    long long bt_stride;
+    long long out_stride;
+    long long num_blocks;
+    int batch;
+    int next_n;
+    int max_context;
+    int n_pad;        // MMA N: next_n*H rounded up to a multiple of 16
+    int stages;       // depth of the K-page ring
+    int epi_groups;   // epilogue warpgroups (1 or 2)
+    int q_box_rows;   // rows one Q load brings (<= n_pad)
+    uint32_t tmem_cols;
+};
+
+struct Bf16Args {
+    const int32_t* context_lengths;
+    const int32_t* requests;
+    const int32_t* block_table;
+    float* scores;
+    unsigned int* status;
+    long long bt_stride;
+    long long scores_stride;
+    long long num_pages;
+    int num_requests;
+    int groups;
+    int group_size;
+    int max_context;
+    int stages;
+    int q_box_rows;
+};
+
+// Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
+size_t fp8_smem_bytes(int n_pad, int next_n, int num_heads, int stages);
+size_t bf16_smem_bytes(int stages);
+
+cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
+                              const Fp8Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
+                               const Bf16Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
+                            cudaStream_t stream);
+
+}  // namespace pml
