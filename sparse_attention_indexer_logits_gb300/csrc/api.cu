@@ -101,13 +101,6 @@ cudaError_t encode_sw128(CUtensorMap& map, CUtensorMapDataType dtype, int rank, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-uint32_t pow2_at_least(uint32_t v)
-{
-    uint32_t p = 32;
-    while (p < v) p <<= 1;
-    return p;
-}
-
 }  // namespace
 
 extern "C" {
@@ -201,14 +194,13 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
     a.batch = batch;
     a.next_n = next_n;
     a.max_context = max_context;
-    a.n_pad = (next_n * num_heads + 15) / 16 * 16;
-    a.epi_groups = next_n >= 2 ? 2 : 1;
-    a.q_box_rows = (int)(rows_total < a.n_pad ? rows_total : a.n_pad);
-    a.tmem_cols = pow2_at_least(2u * a.n_pad);
-    const size_t fixed = fp8_smem_bytes(a.n_pad, next_n, num_heads, 0);
-    const size_t per_stage = fp8_smem_bytes(a.n_pad, next_n, num_heads, 1) - fixed;
+    const int n_pad = (next_n * num_heads + 15) / 16 * 16;
+    a.q_box_rows = (int)(rows_total < n_pad ? rows_total : n_pad);
+    const size_t fixed = fp8_smem_bytes(next_n, num_heads, 0);
+    const size_t per_stage = fp8_smem_bytes(next_n, num_heads, 1) - fixed;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
     if (stages > kMaxFp8Stages) stages = kMaxFp8Stages;
+    stages &= ~1;                        // two producers take even / odd stages
     if (stages < 2) return PML_ERR_UNSUPPORTED;
     a.stages = stages;
 

@@ -93,11 +93,13 @@ struct Walk {
     int b, j;      // current position (b < batch means j < blocks_of(lens[b]))
     int eb, ej;    // end of the range (exclusive)
     int nbb;       // blocks of request b
+    int len;       // length of request b
 
     __device__ __forceinline__ void init(const int32_t* l, int B, int sb, int sj, int e_b, int e_j)
     {
         lens = l; batch = B; b = sb; j = sj; eb = e_b; ej = e_j;
-        nbb = (b < batch) ? blocks_of(__ldg(lens + b)) : 0;
+        len = (b < batch) ? __ldg(lens + b) : 0;
+        nbb = blocks_of(len);
     }
     __device__ __forceinline__ bool done() const { return b >= batch || (b == eb && j == ej); }
     // blocks in the current tile: 1 or 2
@@ -118,18 +120,12 @@ struct Walk {
             j = 0;
             ++b;
             nbb = 0;
-            while (b < batch && (nbb = blocks_of(__ldg(lens + b))) == 0) ++b;
+            while (b < batch && (nbb = blocks_of(len = __ldg(lens + b))) == 0) ++b;
         }
     }
 };
 
-// Per-tile record the producer publishes to the other roles with each stage.
-struct TileInfo {
-    int b;       // request (or group)
-    int j;       // first block of the tile within the request
-    int cnt;     // 1 or 2 blocks
-    int flags;   // kTileFirst | kTileLast | (qslot << 4)
-};
+// Flags of the per-tile records a producer publishes to the other roles.
 constexpr int kTileFirst = 1;   // first tile of a request in this CTA: q / weights were loaded
 constexpr int kTileLast = 2;    // last tile of a request in this CTA: release the q slot after it
 

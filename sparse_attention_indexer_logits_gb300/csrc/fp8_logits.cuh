@@ -1,0 +1,573 @@
+// fp8 paged MQA logits on sm_103a: the kernel template.
+//
+//   out[b*next_n + t, p] = s_p * sum_h w[b*next_n+t, h] * relu(q[b*next_n+t, h] . k_p)
+//
+// ("flashinfer.attn_scores": math block; first bullet -- the rectifier acts
+// per head, before the weighted sum; second bullet -- the fp8 variant is
+// multiplied by the per-token fp32 scale s_p from the trailing scale region
+// of each kv_fused block; note -- row b*next_n+t, empty requests untouched.)
+//
+// One persistent CTA per SM walks a contiguous range of 64-key blocks
+// (common.cuh).  The unit of the MMA is a sub-tile of up to two blocks of one
+// request (128 keys = the MMA's M); a pipeline stage holds KT sub-tiles
+// (KT = 2 when next_n*H <= 128, so that four stages' accumulators still fit
+// TMEM; else 1), so every barrier, descriptor and commit is paid once per 256
+// keys where possible.
+//
+//   warp 0    TMEM allocation and MMA issue: per sub-tile four tcgen05.mma
+//             kind::f8f6f4 (K = 32 each) compute S = K (128 x 128) * Q^T
+//             into the stage's accumulator (TMEM lanes = keys, columns =
+//             next_n*H), one tcgen05.commit per stage.
+//   warps 1-2 producers (whole warps, stages alternate between them).
+//             Block-table entries come 32 at a time in one coalesced load,
+//             double-buffered in registers and handed out by shuffles.  Per
+//             stage the owner waits for the slot, publishes a stage
+//             descriptor (per sub-tile: request, block, count, length,
+//             flags) in shared memory, and lanes 0..3 issue in parallel the
+//             TMA copy of each block's keys (8 KB, 3-D tensor map, 128-byte
+//             swizzle) and the bulk copy of its 64 scales (256 B).  Per
+//             request, the q rows (next_n*H x 128 e4m3) and weights.  After
+//             the last stage an end marker.
+//   warps 3-10 epilogue, two warpgroups.  With KT = 2 group g takes sub-tile
+//             g of every stage (all slots); with KT = 1 both take the one
+//             sub-tile and split the slots (t = g, g+2).  Each thread owns
+//             one key (one TMEM lane), loads its head scores with tcgen05.ld,
+//             rectifies, weights and sums them with eight packed (f32x2)
+//             accumulators, multiplies by s_p and stores, for positions below
+//             min(seq_len, max_context).
+//
+// The MMA and epilogue warps read the stage descriptors instead of walking
+// the schedule, and every loop keeps its stage / accumulator index and phase
+// bit as counters.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pml {
+namespace fp8 {
+
+constexpr int kSubKeyBytes = kTileKeys * kHeadDim;     // 16 KB: one sub-tile of keys
+constexpr int kSubScaleBytes = kTileKeys * 4;          // 512 B
+constexpr int kMmaWarp = 0;
+constexpr int kProducers = 2;                          // warps 1 and 2, alternate stages
+constexpr int kFirstEpiWarp = 1 + kProducers;
+constexpr int kEpiGroups = 2;
+constexpr int kThreads = 32 * kFirstEpiWarp + 128 * kEpiGroups;
+
+__host__ __device__ constexpr int n_pad_of(int next_n, int heads)
+{
+    return (next_n * heads + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int subtiles_of(int n_pad) { return n_pad <= 128 ? 2 : 1; }
+__host__ __device__ constexpr int acc_cols_of(int n_pad) { return subtiles_of(n_pad) * n_pad; }
+__host__ __device__ constexpr int accumulators_of(int n_pad)
+{
+    return acc_cols_of(n_pad) <= 128 ? 4 : 2;
+}
+__host__ __device__ constexpr int tmem_cols_of(int n_pad)
+{
+    return accumulators_of(n_pad) * acc_cols_of(n_pad) <= 32    ? 32
+           : accumulators_of(n_pad) * acc_cols_of(n_pad) <= 64  ? 64
+           : accumulators_of(n_pad) * acc_cols_of(n_pad) <= 128 ? 128
+           : accumulators_of(n_pad) * acc_cols_of(n_pad) <= 256 ? 256
+                                                                : 512;
+}
+
+struct SubDesc {
+    int b;       // request
+    int j;       // first block within the request
+    int cnt;     // blocks (1 or 2); 0 = no sub-tile here
+    int len;     // min(seq_lens[b], max_context)
+    int flags;   // kTileFirst | kTileLast | (q slot << 4)
+    int pad[3];
+};
+
+struct StageDesc {
+    SubDesc sub[2];
+    int end;     // 1: no more work for this CTA
+    int pad[7];
+};
+
+struct Layout {
+    uint32_t k, q, s, w, desc, bar, misc, total;
+    uint32_t q_bytes, w_bytes;
+};
+
+__host__ __device__ inline Layout layout(int n_pad, int next_n, int heads, int stages)
+{
+    const int kt = subtiles_of(n_pad);
+    Layout L;
+    L.q_bytes = (uint32_t)n_pad * kHeadDim;
+    L.w_bytes = (uint32_t)((next_n * heads * 4 + 15) / 16 * 16);
+    L.k = 0;
+    L.q = L.k + (uint32_t)(stages * kt) * kSubKeyBytes;
+    L.s = L.q + 2 * L.q_bytes;
+    L.w = L.s + (uint32_t)(stages * kt) * kSubScaleBytes;
+    L.desc = L.w + 2 * L.w_bytes;
+    L.bar = L.desc + (uint32_t)stages * (uint32_t)sizeof(StageDesc);
+    L.misc = L.bar + (uint32_t)(2 * stages + 12) * 8;
+    L.total = L.misc + 64;
+    return L;
+}
+
+// sum_i w[i] * relu(v[i]) over K values, eight independent packed accumulators.
+template <int K>
+__device__ __forceinline__ float relu_dot(const float (&v)[K], const float4* __restrict__ w4)
+{
+    constexpr int NA = (K / 2) < 8 ? (K / 2) : 8;
+    uint64_t acc[NA];
+#pragma unroll
+    for (int a = 0; a < NA; ++a) acc[a] = 0ull;
+#pragma unroll
+    for (int i = 0; i < K; i += 4) {
+        const float4 w = w4[i / 4];
+        const uint64_t x0 = pack2(fmaxf(v[i], 0.f), fmaxf(v[i + 1], 0.f));
+        const uint64_t x1 = pack2(fmaxf(v[i + 2], 0.f), fmaxf(v[i + 3], 0.f));
+        acc[(i / 2) % NA] = fma2(pack2(w.x, w.y), x0, acc[(i / 2) % NA]);
+        acc[(i / 2 + 1) % NA] = fma2(pack2(w.z, w.w), x1, acc[(i / 2 + 1) % NA]);
+    }
+    float r = 0.f;
+#pragma unroll
+    for (int a = 0; a < NA; ++a) r += sum2(acc[a]);
+    return r;
+}
+
+// One slot's logit (before s_p) for this thread's key: H head scores from
+// TMEM at taddr, rectified, weighted and summed.
+template <int H>
+__device__ __forceinline__ float slot_logit(uint32_t taddr, const float4* __restrict__ w4)
+{
+    if constexpr (H == 64) {
+        float v[64];
+        tmem_ld64(taddr, v);
+        return relu_dot<64>(v, w4);
+    } else if constexpr (H == 32) {
+        float v[32];
+        tmem_ld32(taddr, v);
+        return relu_dot<32>(v, w4);
+    } else if constexpr (H == 16) {
+        float v[16];
+        tmem_ld16(taddr, v);
+        return relu_dot<16>(v, w4);
+    } else {
+        float v[8];
+        tmem_ld8(taddr, v);
+        return relu_dot<8>(v, w4);
+    }
+}
+
+// Position of the block `off` blocks after (pb, pj) in the CTA's walk order;
+// false if that is at or past the range end (eb, ej).
+__device__ __forceinline__ bool block_at(const int32_t* __restrict__ lens, int batch, int pb,
+                                         int pj, int pnb, int eb, int ej, int off, int& ob,
+                                         int& oj)
+{
+    int b = pb, j = pj + off, nb = pnb;
+    while (true) {
+        if (b >= batch) return false;
+        if (j < nb) break;
+        j -= nb;
+        do {
+            ++b;
+        } while (b < batch && (nb = blocks_of(__ldg(lens + b))) == 0);
+    }
+    if (b > eb || (b == eb && j >= ej)) return false;
+    ob = b;
+    oj = j;
+    return true;
+}
+
+template <int H, int NN>
+__global__ void __launch_bounds__(kThreads, 1)
+    logits_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                  const Fp8Args a)
+{
+    constexpr int N = n_pad_of(NN, H);
+    constexpr int KT = subtiles_of(N);
+    constexpr int COLS = acc_cols_of(N);
+    constexpr int NACC = accumulators_of(N);
+    constexpr int NH = NN * H;
+    constexpr uint32_t kStageKeyBytes = KT * kSubKeyBytes;
+    constexpr uint32_t kStageScaleBytes = KT * kSubScaleBytes;
+    constexpr uint32_t kEpiWarps = 4 * kEpiGroups;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int S = a.stages;
+    const Layout L = layout(N, NN, H, S);
+
+    const uint32_t base = smem_addr(smem);
+    const uint32_t k_base = base + L.k;
+    const uint32_t q_base = base + L.q;
+    const uint32_t s_base = base + L.s;
+    const float* scales_smem = reinterpret_cast<const float*>(smem + L.s);
+    StageDesc* descs = reinterpret_cast<StageDesc*>(smem + L.desc);
+    const uint32_t bar = base + L.bar;
+    const uint32_t full_bar0 = bar;                        // + 8*stage
+    const uint32_t empty_bar0 = bar + 8u * S;
+    const uint32_t tfull_bar0 = bar + 8u * (2 * S);        // + 8*acc
+    const uint32_t tempty_bar0 = bar + 8u * (2 * S + 4);
+    const uint32_t qfull_bar0 = bar + 8u * (2 * S + 8);    // + 8*slot
+    const uint32_t qempty_bar0 = bar + 8u * (2 * S + 10);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+    int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---------------------------------------------------------------- setup
+    if (warp == 1) {
+        int sb, sj, eb, ej;
+        if (a.schedule_meta != nullptr) {
+            sb = __ldg(a.schedule_meta + 2 * blockIdx.x);
+            sj = __ldg(a.schedule_meta + 2 * blockIdx.x + 1);
+            eb = __ldg(a.schedule_meta + 2 * blockIdx.x + 2);
+            ej = __ldg(a.schedule_meta + 2 * blockIdx.x + 3);
+        } else {
+            const long long total = warp_total_blocks(a.seq_lens, a.batch);
+            const long long s0 = range_start(total, gridDim.x, blockIdx.x);
+            const long long s1 = range_start(total, gridDim.x, blockIdx.x + 1);
+            warp_locate2(a.seq_lens, a.batch, s0, s1, sb, sj, eb, ej);
+        }
+        if (lane == 0) {
+            sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
+            *abort_flag = 0;
+            for (int s = 0; s < S; ++s) {
+                mbar_init(full_bar0 + 8u * s, 1);
+                mbar_init(empty_bar0 + 8u * s, kEpiWarps);
+            }
+            for (int i = 0; i < 4; ++i) {
+                mbar_init(tfull_bar0 + 8u * i, 1);
+                mbar_init(tempty_bar0 + 8u * i, kEpiWarps);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(qfull_bar0 + 8u * i, 1);
+                mbar_init(qempty_bar0 + 8u * i, kEpiWarps);
+            }
+            fence_mbar_init();
+            tma_prefetch_map(&kmap);
+            tma_prefetch_map(&qmap);
+        }
+    } else if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), tmem_cols_of(N));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp >= 1 && warp <= kProducers) {
+        // ------------------------------------------------------------ producers
+        const int sb = sched[0], sj = sched[1], eb = sched[2], ej = sched[3];
+        const int me = warp - 1;
+        const uint64_t policy = policy_evict_first();
+        Walk w;
+        w.init(a.seq_lens, a.batch, sb, sj, eb, ej);
+        // block-table chunks: lane l of chunk k holds the physical block of the
+        // CTA's (32k + l)-th block (-1 past the range or past max_context)
+        int cb = sb, cj = sj, cnb = w.nbb;
+        bool chunks_left = !w.done();
+        auto load_chunk = [&]() -> int {
+            int phys = -1;
+            if (chunks_left) {
+                int ob, oj;
+                if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, lane, ob, oj) &&
+                    (long long)oj * kBlockKeys < a.max_context)
+                    phys = __ldg(a.block_table + (long long)ob * a.bt_stride + oj);
+                int nb_, nj_;
+                if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, 32, nb_, nj_)) {
+                    cb = nb_; cj = nj_; cnb = blocks_of(__ldg(a.seq_lens + cb));
+                } else {
+                    chunks_left = false;
+                }
+            }
+            return phys;
+        };
+        int phys_cur = load_chunk();
+        int phys_nxt = load_chunk();
+        int g = 0;                      // blocks consumed within the current chunk
+        uint32_t s = (uint32_t)me, ph = 0;
+        int qcount = 0, prev_b = -1, k = 0, my_issued = 0;
+        bool ok = true;
+        while (!w.done()) {
+            const bool mine = (k % kProducers) == me;
+            StageDesc sd;
+            sd.end = 0;
+            // lane l (< 2*KT) copies block slot l of the stage: sub-tile l/2, block l%2
+            int sphys[4] = {0, 0, 0, 0};
+            unsigned smask = 0;
+#pragma unroll
+            for (int i = 0; i < KT; ++i) {
+                sd.sub[i].cnt = 0;
+                sd.sub[i].flags = 0;
+                if (!ok || w.done()) continue;
+                const int c = w.cnt();
+                int flags = 0;
+                if (w.b != prev_b) {
+                    const int slot = qcount & 1;
+                    if (mine) {
+                        if (lane == 0) {
+                            ok = mbar_wait(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1,
+                                           abort_flag, a.status);
+                            if (ok) {
+                                const uint32_t qfb = qfull_bar0 + 8u * slot;
+                                mbar_arrive_expect_tx(qfb,
+                                                      (uint32_t)a.q_box_rows * kHeadDim + NH * 4u);
+                                tma_load_2d(q_base + slot * L.q_bytes, &qmap, qfb, 0, w.b * NH);
+                                bulk_load(base + L.w + slot * L.w_bytes,
+                                          a.weights + (long long)w.b * NH, NH * 4u, qfb);
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                    }
+                    flags |= kTileFirst;
+                    ++qcount;
+                    prev_b = w.b;
+                }
+                flags |= ((qcount - 1) & 1) << 4;
+                if (w.last_of_request(c)) flags |= kTileLast;
+                const int l0 = g, l1 = g + 1;
+                const int v0 = __shfl_sync(0xffffffffu, phys_cur, l0 & 31);
+                const int v0n = __shfl_sync(0xffffffffu, phys_nxt, l0 & 31);
+                const int v1 = __shfl_sync(0xffffffffu, phys_cur, l1 & 31);
+                const int v1n = __shfl_sync(0xffffffffu, phys_nxt, l1 & 31);
+                const int p0 = l0 < 32 ? v0 : v0n;
+                const int p1 = l1 < 32 ? v1 : v1n;
+                g += c;
+                if (g >= 32) {
+                    g -= 32;
+                    phys_cur = phys_nxt;
+                    phys_nxt = load_chunk();
+                }
+                if ((long long)w.j * kBlockKeys < a.max_context) {
+                    sphys[2 * i] = p0;
+                    smask |= 1u << (2 * i);
+                }
+                if (c == 2 && (long long)(w.j + 1) * kBlockKeys < a.max_context) {
+                    sphys[2 * i + 1] = p1;
+                    smask |= 1u << (2 * i + 1);
+                }
+                sd.sub[i].b = w.b;
+                sd.sub[i].j = w.j;
+                sd.sub[i].cnt = c;
+                sd.sub[i].len = min(w.len, a.max_context);
+                sd.sub[i].flags = flags;
+                w.advance(c);
+            }
+            if (!ok) break;
+            if (mine) {
+                if (lane == 0) ok = mbar_wait(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    descs[s] = sd;
+                    mbar_arrive_expect_tx(full_bar0 + 8u * s,
+                                          (uint32_t)__popc(smask) * kFp8BlockBytes);
+                }
+                __syncwarp();
+                if (lane < 2 * KT && ((smask >> lane) & 1u)) {
+                    int pb = lane == 0 ? sphys[0] : lane == 1 ? sphys[1] : lane == 2 ? sphys[2] : sphys[3];
+                    const int bs = lane;
+                    if (pb < 0 || (long long)pb >= a.num_blocks) {
+                        atomicOr(a.status, kStatusBadBlock);
+                        pb = 0;
+                    }
+                    tma_load_3d_stream(k_base + s * kStageKeyBytes + bs * kFp8BlockKeyBytes, &kmap,
+                                       full_bar0 + 8u * s, 0, 0, pb, policy);
+                    bulk_load_stream(s_base + s * kStageScaleBytes + bs * (kBlockKeys * 4),
+                                     a.kv_fused + (long long)pb * kFp8BlockBytes + kFp8BlockKeyBytes,
+                                     kBlockKeys * 4, full_bar0 + 8u * s, policy);
+                }
+                ++my_issued;
+                s += kProducers;
+                if (s >= (uint32_t)S) { s -= S; ph ^= 1; }
+            }
+            ++k;
+        }
+        if (ok && (k % kProducers) == me && lane == 0) {
+            // end marker for the MMA and epilogue warps, in the stage after the last one
+            ok = mbar_wait(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+            if (ok) {
+                descs[s].end = 1;
+                mbar_arrive(full_bar0 + 8u * s);
+            }
+        }
+        if (!ok && lane == 0) {
+            // drain: let every copy this warp issued land before the CTA exits
+            uint32_t ds = s, dph = ph;
+            for (int t = 0; t < my_issued && t < S / kProducers; ++t) {
+                if (ds < (uint32_t)kProducers) { ds += S; dph ^= 1; }
+                ds -= kProducers;
+                mbar_wait_drain(full_bar0 + 8u * ds, dph);
+            }
+            for (int qc = (qcount > 2 ? qcount - 2 : 0); qc < qcount; ++qc)
+                mbar_wait_drain(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(0, 0, kTileKeys, N);
+            uint32_t s = 0, ph = 0, acc = 0, aph = 0;
+            int qcount = 0, done = 0;
+            bool ok = true;
+            while (true) {
+                ok = mbar_wait(full_bar0 + 8u * s, ph, abort_flag, a.status);
+                if (!ok) break;
+                const StageDesc& sd = descs[s];
+                if (sd.end) break;
+                ok = mbar_wait(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < KT; ++i) {
+                    const int cnt = sd.sub[i].cnt;
+                    const int flags = sd.sub[i].flags;
+                    if (cnt == 0 || !ok) continue;
+                    const int slot = (flags >> 4) & 1;
+                    if (flags & kTileFirst) {
+                        ok = mbar_wait(qfull_bar0 + 8u * slot, (qcount >> 1) & 1, abort_flag,
+                                       a.status);
+                        ++qcount;
+                        if (!ok) continue;
+                        tc_fence_after();
+                    }
+                    const uint64_t ad =
+                        smem_desc_sw128(k_base + s * kStageKeyBytes + i * kSubKeyBytes);
+                    const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
+                    const uint32_t dt = tmem_base + acc * COLS + i * N;
+#pragma unroll
+                    for (int kk = 0; kk < kHeadDim / 32; ++kk)
+                        mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar0 + 8u * acc);
+                ++done;
+                if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
+                if (++acc == NACC) { acc = 0; aph ^= 1; }
+            }
+            if (done > 0) {
+                // every MMA issued has completed before TMEM is released
+                const uint32_t la = (acc + NACC - 1) % NACC;
+                const uint32_t lph = (acc == 0) ? (aph ^ 1) : aph;
+                mbar_wait_drain(tfull_bar0 + 8u * la, lph);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int grp = (warp - kFirstEpiWarp) >> 2;
+        const int quad = warp & 3;             // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;      // key row within the sub-tile
+        const int page = row >> 6;
+        const int key = row & 63;
+        const int my_sub = KT == 2 ? grp : 0;
+        constexpr int kSlotStep = KT == 2 ? 1 : 2;
+        const int first_slot = KT == 2 ? 0 : grp;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+        uint32_t s = 0, ph = 0, acc = 0, aph = 0;
+        int qcount = 0;
+        bool ok = true;
+        while (true) {
+            ok = mbar_wait(full_bar0 + 8u * s, ph, abort_flag, a.status);
+            if (!ok) break;
+            const StageDesc& sd = descs[s];
+            if (sd.end) break;
+            // every warp waits for each request's q/weights in order, so that
+            // its release of the slot below can never run a phase ahead
+#pragma unroll
+            for (int i = 0; i < KT; ++i) {
+                if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
+                    ok = mbar_wait(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
+                                   (qcount >> 1) & 1, abort_flag, a.status);
+                    ++qcount;
+                }
+            }
+            if (!ok) break;
+            ok = mbar_wait(tfull_bar0 + 8u * acc, aph, abort_flag, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            const SubDesc d = sd.sub[my_sub];
+            if (d.cnt != 0) {
+                const int pos = (d.j + page) * kBlockKeys + key;
+                const bool valid = page < d.cnt && pos < d.len;
+                const float sp = scales_smem[s * (kStageScaleBytes / 4) + my_sub * kTileKeys + row];
+                const float4* w4 = reinterpret_cast<const float4*>(
+                    smem + L.w + ((d.flags >> 4) & 1) * L.w_bytes);
+                float* orow = a.out + (long long)d.b * NN * a.out_stride + pos;
+                const uint32_t taddr = lane_addr + acc * COLS + my_sub * N;
+#pragma unroll
+                for (int t = first_slot; t < NN; t += kSlotStep) {
+                    const float r = slot_logit<H>(taddr + t * H, w4 + t * (H / 4));
+                    if (valid) orow[(long long)t * a.out_stride] = sp * r;
+                }
+            }
+            int rel0 = -1, rel1 = -1;
+            if (sd.sub[0].cnt != 0 && (sd.sub[0].flags & kTileLast)) rel0 = (sd.sub[0].flags >> 4) & 1;
+            if (KT == 2 && sd.sub[1].cnt != 0 && (sd.sub[1].flags & kTileLast))
+                rel1 = (sd.sub[1].flags >> 4) & 1;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(tempty_bar0 + 8u * acc);
+                mbar_arrive(empty_bar0 + 8u * s);
+                if (rel0 >= 0) mbar_arrive(qempty_bar0 + 8u * rel0);
+                if (rel1 >= 0) mbar_arrive(qempty_bar0 + 8u * rel1);
+            }
+            if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
+            if (++acc == NACC) { acc = 0; aph ^= 1; }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols_of(N));
+    }
+}
+
+template <int H, int NN>
+cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Args& a,
+                   int num_ctas, cudaStream_t stream)
+{
+    constexpr int N = n_pad_of(NN, H);
+    const size_t smem = (size_t)layout(N, NN, H, a.stages).total + 1024;
+    static int configured_device = -1;
+    static size_t configured_smem = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev || configured_smem < smem) {
+        e = cudaFuncSetAttribute(logits_kernel<H, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+        configured_smem = smem;
+    }
+    logits_kernel<H, NN><<<num_ctas, kThreads, smem, stream>>>(kmap, qmap, a);
+    return cudaGetLastError();
+}
+
+template <int H>
+cudaError_t launch_heads(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Args& a,
+                         int num_ctas, cudaStream_t stream)
+{
+    switch (a.next_n) {
+    case 1: return launch<H, 1>(kmap, qmap, a, num_ctas, stream);
+    case 2: return launch<H, 2>(kmap, qmap, a, num_ctas, stream);
+    case 3: return launch<H, 3>(kmap, qmap, a, num_ctas, stream);
+    case 4: return launch<H, 4>(kmap, qmap, a, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fp8
+}  // namespace pml

@@ -22,11 +22,8 @@ struct Fp8Args {
     int batch;
     int next_n;
     int max_context;
-    int n_pad;        // MMA N: next_n*H rounded up to a multiple of 16
     int stages;       // depth of the K-page ring
-    int epi_groups;   // epilogue warpgroups (1 or 2)
-    int q_box_rows;   // rows one Q load brings (<= n_pad)
-    uint32_t tmem_cols;
+    int q_box_rows;   // rows one Q load brings (<= MMA N)
 };
 
 struct Bf16Args {
@@ -47,7 +44,7 @@ struct Bf16Args {
 };
 
 // Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
-size_t fp8_smem_bytes(int n_pad, int next_n, int num_heads, int stages);
+size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
 
 cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
