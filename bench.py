@@ -237,6 +237,19 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def reduce_over_ranks(seconds: float, positions: int, dist, device):
+    """Whole-job timing across ranks: the slowest rank's time and the sum of
+    the positions every rank scored (identity without a process group)."""
+    if dist is None:
+        return seconds, positions
+    t = torch.tensor([seconds, float(positions)], dtype=torch.float64, device=device)
+    tmax = t[:1].clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    psum = t[1:].clone()
+    dist.all_reduce(psum, op=dist.ReduceOp.SUM)
+    return float(tmax.item()), int(psum.item())
+
+
 def config_of(workload, p, world, l2="rotate", copies=3):
     l2_text = (f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)" if l2 == "flush"
                else f"inputs larger than L2: {copies} resident copies of the workload used in "
@@ -367,14 +380,7 @@ def main():
     if status:
         raise SystemExit(f"device status word set during the bench: {status:#x}")
 
-    positions_all = p.positions
-    if dist is not None:
-        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
-        pp = torch.tensor([p.positions], dtype=torch.float64, device=dev)
-        dist.all_reduce(pp, op=dist.ReduceOp.SUM)
-        positions_all = int(pp.item())
+    total_s, positions_all = reduce_over_ranks(total_s, p.positions, dist, dev)
     value = positions_all * args.steps / total_s
     avg_launch_s = total_s / args.steps
 
@@ -421,11 +427,7 @@ def main():
         e2e_step()
     ee.record(stream)
     torch.cuda.synchronize()
-    e2e_s = es.elapsed_time(ee) / 1e3
-    if dist is not None:
-        tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s, _ = reduce_over_ranks(es.elapsed_time(ee) / 1e3, 0, dist, dev)
     e2e = {"value": positions_all * args.e2e_steps / e2e_s, "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
