@@ -156,6 +156,48 @@ int pml_indexer_scores_bf16(const uint16_t* query, int rows, const uint16_t* key
                             const int32_t* context_lengths, const int32_t* requests, int groups,
                             float* scores, int64_t scores_stride, int max_context, void* stream);
 
+/*
+ * pml_fp8_paged_mqa_logits_noalloc -- the two-step call (pml_schedule, then
+ * pml_fp8_paged_mqa_logits with that schedule) for callers that cannot
+ * allocate device memory.  The documentation pages have no counterpart: it
+ * exists for this library's users.
+ *
+ * Who needs it: code that only receives the buffers it works on and has no
+ * way to obtain more device memory -- a plugin inside a host runtime that owns
+ * all allocations, a serving loop running under a memory pool that forbids
+ * raw cudaMalloc (which also synchronises the device), or a C caller with no
+ * allocator at hand.  The regular two-step path needs such a caller to find
+ * room for the (num_ctas+1)*2 int32 schedule; here the schedule lives in a
+ * fixed array inside the library's own device memory (8200 bytes, held on
+ * every device that loads the library until the process exits).
+ *
+ * Arguments and results are those of pml_fp8_paged_mqa_logits without
+ * schedule_meta.  num_ctas: 0 = pml_default_num_ctas (capped at the limit),
+ * at most pml_noalloc_max_ctas() = 1024; larger values return
+ * PML_ERR_INVALID_ARG and launch nothing.  Nothing is allocated or freed: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  A failure there returns PML_ERR_CUDA.
+ *
+ * All calls share the one array, which keeps the last call's schedule; each
+ * call rewrites every entry it reads, so nothing needs clearing.  Calls whose
+ * work overlaps on the GPU (different streams, no ordering between them) race
+ * on the array: order them, or use the regular entry points with separate
+ * buffers.  If the logits launch is rejected after the schedule was written,
+ * the only side effect is the rewritten array.
+ */
+int pml_fp8_paged_mqa_logits_noalloc(const uint8_t* q, const uint8_t* kv_fused,
+                                     int64_t num_blocks, const float* weights,
+                                     const int32_t* seq_lens, const int32_t* block_table,
+                                     int64_t bt_stride, int num_ctas, float* out,
+                                     int64_t out_stride, int max_context, int batch, int next_n,
+                                     int num_heads, void* stream);
+
+/* Largest num_ctas pml_fp8_paged_mqa_logits_noalloc accepts (1024). */
+int pml_noalloc_max_ctas(void);
+
 /* Read (and, if clear != 0, reset) the current device's sticky status word.
  * Synchronises with the device (waits for all work queued so far). */
 int pml_device_status(unsigned int* status, int clear);

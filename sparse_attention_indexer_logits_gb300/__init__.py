@@ -27,8 +27,8 @@ import torch
 
 __all__ = [
     "PmlError", "lib", "library_path", "pml_schedule", "pml_fp8_paged_mqa_logits",
-    "pml_indexer_scores_bf16", "pml_device_status", "pml_default_num_ctas",
-    "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
+    "pml_indexer_scores_bf16", "pml_fp8_paged_mqa_logits_noalloc", "pml_device_status",
+    "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
     "fp8_paged_mqa_logits", "indexer_scores", "compute_paged_mqa_logits_schedule",
 ]
 
@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
         L.pml_indexer_scores_bf16.argtypes = [P, i32, P, i64, i64, P, i64, i32, P, P, i32, P, i64,
                                               i32, P]
         L.pml_indexer_scores_bf16.restype = i32
+        L.pml_fp8_paged_mqa_logits_noalloc.argtypes = [P, P, i64, P, P, P, i64, i32, P, i64, i32,
+                                                       i32, i32, i32, P]
+        L.pml_fp8_paged_mqa_logits_noalloc.restype = i32
+        L.pml_noalloc_max_ctas.restype = i32
         L.pml_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.pml_device_status.restype = i32
         _lib = L
@@ -212,6 +216,25 @@ def pml_indexer_scores_bf16(query: torch.Tensor, key_cache: torch.Tensor, page_s
         _ptr(requests), context_lengths.numel(), _ptr(scores), scores.stride(0), max_context,
         _stream(stream)), "pml_indexer_scores_bf16")
     return scores
+
+
+def pml_fp8_paged_mqa_logits_noalloc(q: torch.Tensor, kv_fused: torch.Tensor,
+                                     weights: torch.Tensor, seq_lens: torch.Tensor,
+                                     block_table: torch.Tensor, out: torch.Tensor, max_context: int,
+                                     next_n: int, num_ctas: int = 0, stream=None) -> torch.Tensor:
+    """Same result as ``pml_fp8_paged_mqa_logits`` with a GPU-computed schedule
+    kept in the library's own fixed device array (no device allocation by the
+    library; see include/pml.h for the sharing rules).  Arguments as there."""
+    for t, nm in ((q, "q"), (kv_fused, "kv_fused"), (weights, "weights"), (seq_lens, "seq_lens")):
+        _cuda(t, nm)
+    _cuda(block_table, "block_table", contiguous=False)
+    _cuda(out, "out", contiguous=False)
+    batch = seq_lens.numel()
+    _check(lib().pml_fp8_paged_mqa_logits_noalloc(
+        _ptr(q), _ptr(kv_fused), kv_fused.numel() // 8448, _ptr(weights), _ptr(seq_lens),
+        _ptr(block_table), block_table.stride(0), num_ctas, _ptr(out), out.stride(0), max_context,
+        batch, next_n, q.shape[1], _stream(stream)), "pml_fp8_paged_mqa_logits_noalloc")
+    return out
 
 
 # ---------------------------------------------------------------- pages' keyword style
