@@ -14,10 +14,10 @@
 // TMEM; else 1), so every barrier, descriptor and commit is paid once per 256
 // keys where possible.
 //
-//   warp 0    TMEM allocation and MMA issue: per sub-tile four tcgen05.mma
-//             kind::f8f6f4 (K = 32 each) compute S = K (128 x 128) * Q^T
-//             into the stage's accumulator (TMEM lanes = keys, columns =
-//             next_n*H), one tcgen05.commit per stage.
+//   warps 0,3 MMA issue (warp 0 also allocates TMEM): warp m takes sub-tile
+//             m of every stage; four tcgen05.mma kind::f8f6f4 (K = 32 each)
+//             compute S = K (128 x 128) * Q^T into the stage's accumulator
+//             (TMEM lanes = keys, columns = next_n*H), then tcgen05.commit.
 //   warps 1-2 producers (whole warps, stages alternate between them).
 //             Block-table entries come 32 at a time in one coalesced load,
 //             double-buffered in registers and handed out by shuffles.  Per
@@ -28,12 +28,13 @@
 //             swizzle) and the bulk copy of its 64 scales (256 B).  Per
 //             request, the q rows (next_n*H x 128 e4m3) and weights.  After
 //             the last stage an end marker.
-//   warps 3-10 epilogue, two warpgroups.  With KT = 2 group g takes sub-tile
-//             g of every stage (all slots); with KT = 1 both take the one
-//             sub-tile and split the slots (t = g, g+2).  Each thread owns
-//             one key (one TMEM lane), loads its head scores with tcgen05.ld,
-//             rectifies, weights and sums them with eight packed (f32x2)
-//             accumulators, multiplies by s_p and stores, for positions below
+//   warps 4-11 epilogue, two warpgroups: with KT = 2 group g takes sub-tile g
+//             of every stage (all slots), with KT = 1 both take the one
+//             sub-tile and split the slots (t = g, g+2).  Each thread owns one
+//             key (one TMEM lane), reads its head scores with tcgen05.ld in
+//             chunks of 32 columns (the next chunk in flight while the current
+//             one is computed), rectifies, weights and sums them with packed
+//             f32x2 FMAs, multiplies by s_p and stores, for positions below
 //             min(seq_len, max_context).
 //
 // The MMA and epilogue warps read the stage descriptors instead of walking
@@ -53,11 +54,17 @@ namespace fp8 {
 
 constexpr int kSubKeyBytes = kTileKeys * kHeadDim;     // 16 KB: one sub-tile of keys
 constexpr int kSubScaleBytes = kTileKeys * 4;          // 512 B
-constexpr int kMmaWarp = 0;
+constexpr int kMmaWarp = 0;                            // also allocates TMEM
 constexpr int kProducers = 2;                          // warps 1 and 2, alternate stages
-constexpr int kFirstEpiWarp = 1 + kProducers;
-constexpr int kEpiGroups = 2;
-constexpr int kThreads = 32 * kFirstEpiWarp + 128 * kEpiGroups;
+constexpr int kMmaWarp2 = 3;                           // issues sub-tile 1 of each stage
+constexpr int kFirstEpiWarp = 4;
+// Two epilogue warpgroups: one per sub-tile when a stage holds two, else
+// both on the one sub-tile with the slots split between them.
+__host__ __device__ constexpr int epi_groups_of(int) { return 2; }
+__host__ __device__ constexpr int threads_of(int next_n)
+{
+    return 32 * kFirstEpiWarp + 128 * epi_groups_of(next_n);
+}
 
 __host__ __device__ constexpr int n_pad_of(int next_n, int heads)
 {
@@ -115,49 +122,68 @@ __host__ __device__ inline Layout layout(int n_pad, int next_n, int heads, int s
     return L;
 }
 
-// sum_i w[i] * relu(v[i]) over K values, eight independent packed accumulators.
-template <int K>
-__device__ __forceinline__ float relu_dot(const float (&v)[K], const float4* __restrict__ w4)
+template <int W>
+__device__ __forceinline__ void tmem_ld_async(uint32_t taddr, uint32_t (&r)[W])
 {
-    constexpr int NA = (K / 2) < 8 ? (K / 2) : 8;
-    uint64_t acc[NA];
-#pragma unroll
-    for (int a = 0; a < NA; ++a) acc[a] = 0ull;
-#pragma unroll
-    for (int i = 0; i < K; i += 4) {
-        const float4 w = w4[i / 4];
-        const uint64_t x0 = pack2(fmaxf(v[i], 0.f), fmaxf(v[i + 1], 0.f));
-        const uint64_t x1 = pack2(fmaxf(v[i + 2], 0.f), fmaxf(v[i + 3], 0.f));
-        acc[(i / 2) % NA] = fma2(pack2(w.x, w.y), x0, acc[(i / 2) % NA]);
-        acc[(i / 2 + 1) % NA] = fma2(pack2(w.z, w.w), x1, acc[(i / 2 + 1) % NA]);
-    }
-    float r = 0.f;
-#pragma unroll
-    for (int a = 0; a < NA; ++a) r += sum2(acc[a]);
-    return r;
+    if constexpr (W == 32) tmem_ld32_async(taddr, r);
+    else if constexpr (W == 16) tmem_ld16_async(taddr, r);
+    else tmem_ld8_async(taddr, r);
 }
 
-// One slot's logit (before s_p) for this thread's key: H head scores from
-// TMEM at taddr, rectified, weighted and summed.
-template <int H>
-__device__ __forceinline__ float slot_logit(uint32_t taddr, const float4* __restrict__ w4)
+template <int W>
+__device__ __forceinline__ void tmem_wait_bind(uint32_t (&r)[W])
 {
-    if constexpr (H == 64) {
-        float v[64];
-        tmem_ld64(taddr, v);
-        return relu_dot<64>(v, w4);
-    } else if constexpr (H == 32) {
-        float v[32];
-        tmem_ld32(taddr, v);
-        return relu_dot<32>(v, w4);
-    } else if constexpr (H == 16) {
-        float v[16];
-        tmem_ld16(taddr, v);
-        return relu_dot<16>(v, w4);
-    } else {
-        float v[8];
-        tmem_ld8(taddr, v);
-        return relu_dot<8>(v, w4);
+    if constexpr (W == 32) tmem_wait_bind32(r);
+    else if constexpr (W == 16) tmem_wait_bind16(r);
+    else tmem_wait_bind8(r);
+}
+
+// The logits of this thread's key for its SL slots t = first_slot + k*GS
+// (k < SL, t < NN): the head scores are read from TMEM in chunks of up to 32
+// columns, the load of the next chunk issued before the current one is
+// rectified, weighted (packed f32x2 FMAs, eight lanes of accumulators) and
+// summed, so TMEM latency hides behind the arithmetic.  taddr0 is the column
+// of slot 0 in this thread's lane, w4 the slot-0 weights.
+template <int H, int NN, int SL, int GS>
+__device__ __forceinline__ void slot_logits(uint32_t taddr0, const float4* __restrict__ w4,
+                                            int first_slot, float sp, bool valid,
+                                            float* __restrict__ orow, long long out_stride)
+{
+    constexpr int CW = H >= 32 ? 32 : H;    // chunk width (columns)
+    constexpr int CPS = H / CW;             // chunks per slot
+    constexpr int NC = SL * CPS;
+    uint32_t buf[2][CW];
+    uint64_t acc[4];
+    tmem_ld_async<CW>(taddr0 + first_slot * H, buf[0]);
+    tmem_wait_bind<CW>(buf[0]);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int t = first_slot + (c / CPS) * GS;
+        if (c % CPS == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) acc[a] = 0ull;
+        }
+        if (c + 1 < NC) {
+            const int tn = first_slot + ((c + 1) / CPS) * GS;
+            tmem_ld_async<CW>(taddr0 + tn * H + ((c + 1) % CPS) * CW, buf[(c + 1) & 1]);
+        }
+        const float4* wc = w4 + t * (H / 4) + (c % CPS) * (CW / 4);
+        const uint32_t(&v)[CW] = buf[c & 1];
+#pragma unroll
+        for (int i = 0; i < CW; i += 4) {
+            const float4 w = wc[i / 4];
+            const uint64_t x0 = pack2(fmaxf(__uint_as_float(v[i]), 0.f),
+                                      fmaxf(__uint_as_float(v[i + 1]), 0.f));
+            const uint64_t x1 = pack2(fmaxf(__uint_as_float(v[i + 2]), 0.f),
+                                      fmaxf(__uint_as_float(v[i + 3]), 0.f));
+            acc[(i / 2) % 4] = fma2(pack2(w.x, w.y), x0, acc[(i / 2) % 4]);
+            acc[(i / 2 + 1) % 4] = fma2(pack2(w.z, w.w), x1, acc[(i / 2 + 1) % 4]);
+        }
+        if (c % CPS == CPS - 1) {
+            const float r = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
+            if (valid && t < NN) orow[(long long)t * out_stride] = sp * r;
+        }
+        if (c + 1 < NC) tmem_wait_bind<CW>(buf[(c + 1) & 1]);
     }
 }
 
@@ -183,7 +209,7 @@ __device__ __forceinline__ bool block_at(const int32_t* __restrict__ lens, int b
 }
 
 template <int H, int NN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(NN), 1)
     logits_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                   const Fp8Args a)
 {
@@ -194,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NH = NN * H;
     constexpr uint32_t kStageKeyBytes = KT * kSubKeyBytes;
     constexpr uint32_t kStageScaleBytes = KT * kSubScaleBytes;
-    constexpr uint32_t kEpiWarps = 4 * kEpiGroups;
+    constexpr int EG = epi_groups_of(NN);
+    constexpr uint32_t kEpiWarps = 4 * EG;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -244,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(empty_bar0 + 8u * s, kEpiWarps);
             }
             for (int i = 0; i < 4; ++i) {
-                mbar_init(tfull_bar0 + 8u * i, 1);
+                mbar_init(tfull_bar0 + 8u * i, KT);   // one commit per sub-tile
                 mbar_init(tempty_bar0 + 8u * i, kEpiWarps);
             }
             for (int i = 0; i < 2; ++i) {
@@ -411,11 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int qc = (qcount > 2 ? qcount - 2 : 0); qc < qcount; ++qc)
                 mbar_wait_drain(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ------------------------------------------------------------ MMA issuers
+        // MMA warp m issues sub-tile m of every stage (one tcgen05.mma takes a
+        // thread more cycles to issue than the tensor pipe needs to run it at
+        // these N, so two issuers run in parallel when a stage has two).
+        const int mw = warp == kMmaWarp ? 0 : 1;
+        if (lane == 0 && mw < KT) {
             constexpr uint32_t idesc = make_idesc(0, 0, kTileKeys, N);
-            uint32_t s = 0, ph = 0, acc = 0, aph = 0;
+            uint32_t s = 0, ph = 0, acc = 0, aph = 0, last_acc = 0, last_ph = 0;
             int qcount = 0, done = 0;
             bool ok = true;
             while (true) {
@@ -425,39 +456,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sd.end) break;
                 ok = mbar_wait(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
                 if (!ok) break;
-                tc_fence_after();
+                // q / weights of every request that starts in this stage, in order
 #pragma unroll
                 for (int i = 0; i < KT; ++i) {
-                    const int cnt = sd.sub[i].cnt;
-                    const int flags = sd.sub[i].flags;
-                    if (cnt == 0 || !ok) continue;
-                    const int slot = (flags >> 4) & 1;
-                    if (flags & kTileFirst) {
-                        ok = mbar_wait(qfull_bar0 + 8u * slot, (qcount >> 1) & 1, abort_flag,
-                                       a.status);
+                    if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
+                        ok = mbar_wait(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
+                                       (qcount >> 1) & 1, abort_flag, a.status);
                         ++qcount;
-                        if (!ok) continue;
-                        tc_fence_after();
                     }
+                }
+                if (!ok) break;
+                tc_fence_after();
+                const int cnt = sd.sub[mw].cnt;
+                if (cnt != 0) {
+                    const int slot = (sd.sub[mw].flags >> 4) & 1;
                     const uint64_t ad =
-                        smem_desc_sw128(k_base + s * kStageKeyBytes + i * kSubKeyBytes);
+                        smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
                     const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
-                    const uint32_t dt = tmem_base + acc * COLS + i * N;
+                    const uint32_t dt = tmem_base + acc * COLS + mw * N;
 #pragma unroll
                     for (int kk = 0; kk < kHeadDim / 32; ++kk)
                         mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                    mma_commit(tfull_bar0 + 8u * acc);
+                    last_acc = acc;
+                    last_ph = aph;
+                    ++done;
+                } else {
+                    mbar_arrive(tfull_bar0 + 8u * acc);   // nothing issued for this sub-tile
                 }
-                if (!ok) break;
-                mma_commit(tfull_bar0 + 8u * acc);
-                ++done;
                 if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
                 if (++acc == NACC) { acc = 0; aph ^= 1; }
             }
             if (done > 0) {
-                // every MMA issued has completed before TMEM is released
-                const uint32_t la = (acc + NACC - 1) % NACC;
-                const uint32_t lph = (acc == 0) ? (aph ^ 1) : aph;
-                mbar_wait_drain(tfull_bar0 + 8u * la, lph);
+                // every MMA this warp issued has completed before TMEM is
+                // released: the phase of its last commit completes only then
+                mbar_wait_drain(tfull_bar0 + 8u * last_acc, last_ph);
             }
         }
     } else {
@@ -467,9 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;      // key row within the sub-tile
         const int page = row >> 6;
         const int key = row & 63;
-        const int my_sub = KT == 2 ? grp : 0;
-        constexpr int kSlotStep = KT == 2 ? 1 : 2;
-        const int first_slot = KT == 2 ? 0 : grp;
+        // groups per sub-tile; group g takes sub-tile g / GS and slots t = g % GS (mod GS)
+        constexpr int GS = EG / KT;
+        constexpr int SL = (NN + GS - 1) / GS;   // slots per warp
+        const int my_sub = grp / GS;
+        const int first_slot = grp % GS;
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         uint32_t s = 0, ph = 0, acc = 0, aph = 0;
         int qcount = 0;
@@ -493,30 +528,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(tfull_bar0 + 8u * acc, aph, abort_flag, a.status);
             if (!ok) break;
             tc_fence_after();
+            // The MMAs of this stage are complete, so its key buffers are no
+            // longer read: take the descriptor fields and this key's scale
+            // into registers and hand the stage back to the producers before
+            // the arithmetic, which then overlaps with the next copies.
             const SubDesc d = sd.sub[my_sub];
-            if (d.cnt != 0) {
-                const int pos = (d.j + page) * kBlockKeys + key;
-                const bool valid = page < d.cnt && pos < d.len;
-                const float sp = scales_smem[s * (kStageScaleBytes / 4) + my_sub * kTileKeys + row];
-                const float4* w4 = reinterpret_cast<const float4*>(
-                    smem + L.w + ((d.flags >> 4) & 1) * L.w_bytes);
-                float* orow = a.out + (long long)d.b * NN * a.out_stride + pos;
-                const uint32_t taddr = lane_addr + acc * COLS + my_sub * N;
-#pragma unroll
-                for (int t = first_slot; t < NN; t += kSlotStep) {
-                    const float r = slot_logit<H>(taddr + t * H, w4 + t * (H / 4));
-                    if (valid) orow[(long long)t * a.out_stride] = sp * r;
-                }
-            }
+            const float sp = scales_smem[s * (kStageScaleBytes / 4) + my_sub * kTileKeys + row];
             int rel0 = -1, rel1 = -1;
             if (sd.sub[0].cnt != 0 && (sd.sub[0].flags & kTileLast)) rel0 = (sd.sub[0].flags >> 4) & 1;
             if (KT == 2 && sd.sub[1].cnt != 0 && (sd.sub[1].flags & kTileLast))
                 rel1 = (sd.sub[1].flags >> 4) & 1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar0 + 8u * s);
+            if (d.cnt != 0) {
+                const int pos = (d.j + page) * kBlockKeys + key;
+                const bool valid = page < d.cnt && pos < d.len;
+                const float4* w4 = reinterpret_cast<const float4*>(
+                    smem + L.w + ((d.flags >> 4) & 1) * L.w_bytes);
+                float* orow = a.out + (long long)d.b * NN * a.out_stride + pos;
+                slot_logits<H, NN, SL, GS>(lane_addr + acc * COLS + my_sub * N, w4, first_slot,
+                                           sp, valid, orow, a.out_stride);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(tempty_bar0 + 8u * acc);
-                mbar_arrive(empty_bar0 + 8u * s);
                 if (rel0 >= 0) mbar_arrive(qempty_bar0 + 8u * rel0);
                 if (rel1 >= 0) mbar_arrive(qempty_bar0 + 8u * rel1);
             }
@@ -552,7 +588,7 @@ cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Ar
         configured_device = dev;
         configured_smem = smem;
     }
-    logits_kernel<H, NN><<<num_ctas, kThreads, smem, stream>>>(kmap, qmap, a);
+    logits_kernel<H, NN><<<num_ctas, threads_of(NN), smem, stream>>>(kmap, qmap, a);
     return cudaGetLastError();
 }
 
