@@ -244,14 +244,43 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
     const uint32_t qempty_bar0 = bar + 8u * (2 * S + 10);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
-    int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     // ---------------------------------------------------------------- setup
-    if (warp == 1) {
-        int sb, sj, eb, ej;
+    // The next call may be placed on SMs as this grid leaves them; nothing
+    // here touches global memory before grid_dependency_wait.
+    allow_dependent_launch();
+    const bool producer = warp >= 1 && warp <= kProducers;
+    // Producer state.  The producers compute their range and issue the first
+    // block-table loads before the CTA-wide barrier, so that these global
+    // round trips overlap the TMEM allocation and the barrier set-up.
+    int sb = 0, sj = 0, eb = 0, ej = 0;
+    Walk w;
+    // block-table chunks: lane l of chunk k holds the physical block of the
+    // CTA's (32k + l)-th block (-1 past the range or past max_context)
+    int cb = 0, cj = 0, cnb = 0;
+    bool chunks_left = false;
+    auto load_chunk = [&]() -> int {
+        int phys = -1;
+        if (chunks_left) {
+            int ob, oj;
+            if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, lane, ob, oj) &&
+                (long long)oj * kBlockKeys < a.max_context)
+                phys = __ldg(a.block_table + (long long)ob * a.bt_stride + oj);
+            int nb_, nj_;
+            if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, 32, nb_, nj_)) {
+                cb = nb_; cj = nj_; cnb = blocks_of(__ldg(a.seq_lens + cb));
+            } else {
+                chunks_left = false;
+            }
+        }
+        return phys;
+    };
+    int phys_cur = -1, phys_nxt = -1;
+    if (producer) {
+        grid_dependency_wait();
         if (a.schedule_meta != nullptr) {
             sb = __ldg(a.schedule_meta + 2 * blockIdx.x);
             sj = __ldg(a.schedule_meta + 2 * blockIdx.x + 1);
@@ -263,63 +292,42 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             const long long s1 = range_start(total, gridDim.x, blockIdx.x + 1);
             warp_locate2(a.seq_lens, a.batch, s0, s1, sb, sj, eb, ej);
         }
-        if (lane == 0) {
-            sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
-            *abort_flag = 0;
-            for (int s = 0; s < S; ++s) {
-                mbar_init(full_bar0 + 8u * s, 1);
-                mbar_init(empty_bar0 + 8u * s, kEpiWarps);
-            }
-            for (int i = 0; i < 4; ++i) {
-                mbar_init(tfull_bar0 + 8u * i, KT);   // one commit per sub-tile
-                mbar_init(tempty_bar0 + 8u * i, kEpiWarps);
-            }
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(qfull_bar0 + 8u * i, 1);
-                mbar_init(qempty_bar0 + 8u * i, kEpiWarps);
-            }
-            fence_mbar_init();
-            tma_prefetch_map(&kmap);
-            tma_prefetch_map(&qmap);
-        }
+        w.init(a.seq_lens, a.batch, sb, sj, eb, ej);
+        cb = sb; cj = sj; cnb = w.nbb;
+        chunks_left = !w.done();
+        phys_cur = load_chunk();
+        phys_nxt = load_chunk();
     } else if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), tmem_cols_of(N));
         tmem_relinquish();
+    } else if (warp == kMmaWarp2 && lane == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar0 + 8u * s, 1);
+            mbar_init(empty_bar0 + 8u * s, kEpiWarps);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(tfull_bar0 + 8u * i, KT);   // one commit per sub-tile
+            mbar_init(tempty_bar0 + 8u * i, kEpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull_bar0 + 8u * i, 1);
+            mbar_init(qempty_bar0 + 8u * i, kEpiWarps);
+        }
+        fence_mbar_init();
+        tma_prefetch_map(&kmap);
+        tma_prefetch_map(&qmap);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
 
-    if (warp >= 1 && warp <= kProducers) {
+    if (producer) {
         // ------------------------------------------------------------ producers
-        const int sb = sched[0], sj = sched[1], eb = sched[2], ej = sched[3];
         const int me = warp - 1;
         const uint64_t policy = policy_evict_first();
-        Walk w;
-        w.init(a.seq_lens, a.batch, sb, sj, eb, ej);
-        // block-table chunks: lane l of chunk k holds the physical block of the
-        // CTA's (32k + l)-th block (-1 past the range or past max_context)
-        int cb = sb, cj = sj, cnb = w.nbb;
-        bool chunks_left = !w.done();
-        auto load_chunk = [&]() -> int {
-            int phys = -1;
-            if (chunks_left) {
-                int ob, oj;
-                if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, lane, ob, oj) &&
-                    (long long)oj * kBlockKeys < a.max_context)
-                    phys = __ldg(a.block_table + (long long)ob * a.bt_stride + oj);
-                int nb_, nj_;
-                if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, 32, nb_, nj_)) {
-                    cb = nb_; cj = nj_; cnb = blocks_of(__ldg(a.seq_lens + cb));
-                } else {
-                    chunks_left = false;
-                }
-            }
-            return phys;
-        };
-        int phys_cur = load_chunk();
-        int phys_nxt = load_chunk();
         int g = 0;                      // blocks consumed within the current chunk
         uint32_t s = (uint32_t)me, ph = 0;
         int qcount = 0, prev_b = -1, k = 0, my_issued = 0;
@@ -588,7 +596,20 @@ cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Ar
         configured_device = dev;
         configured_smem = smem;
     }
-    logits_kernel<H, NN><<<num_ctas, threads_of(NN), smem, stream>>>(kmap, qmap, a);
+    // programmatic stream serialization: this launch may begin while the
+    // previous kernel in the stream finishes (see grid_dependency_wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_ctas);
+    cfg.blockDim = dim3((unsigned)threads_of(NN));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, logits_kernel<H, NN>, kmap, qmap, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

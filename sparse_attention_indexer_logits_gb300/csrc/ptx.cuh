@@ -25,6 +25,24 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled onto SMs this grid has left; it still waits in
+// grid_dependency_wait for this grid to complete.
+__device__ __forceinline__ void allow_dependent_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until every grid this one depends on has completed and its memory
+// operations are visible.  Must precede any global read of inputs or write of
+// outputs.  A no-op when the kernel was launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
