@@ -21,6 +21,7 @@ constexpr int kFp8BlockKeyBytes = kBlockKeys * kHeadDim;          // 8192
 constexpr int kFp8BlockBytes = kFp8BlockKeyBytes + kBlockKeys * 4; // 8448: keys, then scales
 constexpr int kTileKeys = 128;                // MMA M: two blocks
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+constexpr unsigned int kWaitSuspendNs = 1000;   // longest hardware suspension per try_wait
 
 // Bits of the device status word (sticky until cleared by the host).
 constexpr unsigned int kStatusWaitTimeout = 1u;   // an mbarrier wait ran out; the CTA aborted

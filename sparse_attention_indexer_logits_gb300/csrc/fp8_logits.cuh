@@ -138,19 +138,21 @@ __device__ __forceinline__ void tmem_wait_bind(uint32_t (&r)[W])
     else tmem_wait_bind8(r);
 }
 
-// The logits of this thread's key for its SL slots t = first_slot + k*GS
-// (k < SL, t < NN): the head scores are read from TMEM in chunks of up to 32
+// The logits of this thread's key for SL slots t = first_slot + k*GS
+// (k < SL): the head scores are read from TMEM in chunks of up to CWMAX
 // columns, the load of the next chunk issued before the current one is
 // rectified, weighted (packed f32x2 FMAs, eight lanes of accumulators) and
 // summed, so TMEM latency hides behind the arithmetic.  taddr0 is the column
-// of slot 0 in this thread's lane, w4 the slot-0 weights.
-template <int H, int NN, int SL, int GS>
-__device__ __forceinline__ void slot_logits(uint32_t taddr0, const float4* __restrict__ w4,
+// of slot 0 in this thread's lane; wp holds the weights of the SL slots as
+// packed pairs (heads 2i, 2i+1 of slot k at wp[k*H/2 + i]).
+template <int H, int SL, int GS, int CWMAX, int WN>
+__device__ __forceinline__ void slot_logits(uint32_t taddr0, const uint64_t (&wp)[WN],
                                             int first_slot, float sp, bool valid,
                                             float* __restrict__ orow, long long out_stride)
 {
-    constexpr int CW = H >= 32 ? 32 : H;    // chunk width (columns)
-    constexpr int CPS = H / CW;             // chunks per slot
+    static_assert(SL * H / 2 <= WN, "weights of every slot are held");
+    constexpr int CW = H >= CWMAX ? CWMAX : H;   // chunk width (columns)
+    constexpr int CPS = H / CW;                  // chunks per slot
     constexpr int NC = SL * CPS;
     uint32_t buf[2][CW];
     uint64_t acc[4];
@@ -158,7 +160,8 @@ __device__ __forceinline__ void slot_logits(uint32_t taddr0, const float4* __res
     tmem_wait_bind<CW>(buf[0]);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        const int t = first_slot + (c / CPS) * GS;
+        const int k = c / CPS;
+        const int t = first_slot + k * GS;
         if (c % CPS == 0) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) acc[a] = 0ull;
@@ -167,25 +170,48 @@ __device__ __forceinline__ void slot_logits(uint32_t taddr0, const float4* __res
             const int tn = first_slot + ((c + 1) / CPS) * GS;
             tmem_ld_async<CW>(taddr0 + tn * H + ((c + 1) % CPS) * CW, buf[(c + 1) & 1]);
         }
-        const float4* wc = w4 + t * (H / 4) + (c % CPS) * (CW / 4);
         const uint32_t(&v)[CW] = buf[c & 1];
+        const int w0 = (k * H + (c % CPS) * CW) / 2;
 #pragma unroll
-        for (int i = 0; i < CW; i += 4) {
-            const float4 w = wc[i / 4];
-            const uint64_t x0 = pack2(fmaxf(__uint_as_float(v[i]), 0.f),
-                                      fmaxf(__uint_as_float(v[i + 1]), 0.f));
-            const uint64_t x1 = pack2(fmaxf(__uint_as_float(v[i + 2]), 0.f),
-                                      fmaxf(__uint_as_float(v[i + 3]), 0.f));
-            acc[(i / 2) % 4] = fma2(pack2(w.x, w.y), x0, acc[(i / 2) % 4]);
-            acc[(i / 2 + 1) % 4] = fma2(pack2(w.z, w.w), x1, acc[(i / 2 + 1) % 4]);
+        for (int i = 0; i < CW; i += 2) {
+            const uint64_t x = pack2(fmaxf(__uint_as_float(v[i]), 0.f),
+                                     fmaxf(__uint_as_float(v[i + 1]), 0.f));
+            acc[(i / 2) % 4] = fma2(wp[w0 + i / 2], x, acc[(i / 2) % 4]);
         }
         if (c % CPS == CPS - 1) {
             const float r = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
-            if (valid && t < NN) orow[(long long)t * out_stride] = sp * r;
+            if (valid) orow[(long long)t * out_stride] = sp * r;
         }
         if (c + 1 < NC) tmem_wait_bind<CW>(buf[(c + 1) & 1]);
     }
 }
+
+// How the two epilogue warpgroups share a stage.  Sub-tile split: group g
+// takes sub-tile g (all slots); slot split: group g takes slots t = g, g+2 of
+// every sub-tile.  A warp keeps the weights of its slots (SL x H) in
+// registers, loaded when its request changes rather than read from shared
+// memory for every key: the split is the one that keeps them to 64 where it
+// can.  Only with next_n*H > 128 at one sub-tile per stage (H = 64,
+// next_n >= 3) are there 128; then the CTA's registers are re-split, the
+// MMA/producer warpgroup dropping to kLowRegs so that the two epilogue
+// warpgroups can hold kHighRegs each (128 x 64 + 256 x 216 = 63488, within
+// the 384 x 168 registers of the block).  ptxas allocates each warpgroup's
+// branch within its budget only if no call (a non-inlined function) sits in
+// it, which is why the waits are fully inlined.
+template <int H, int NN>
+struct EpiPlan {
+    static constexpr int KT = subtiles_of(n_pad_of(NN, H));
+    static constexpr bool kSubSplit = KT == 2 && (NN * H <= 64 || (NN + 1) / 2 * H > 64);
+    static constexpr int GS = kSubSplit ? 1 : 2;            // slot stride
+    static constexpr int SL = (NN + GS - 1) / GS;           // slots of group 0
+    static constexpr int kWeightPairs = SL * H / 2;
+    static constexpr bool kSplitRegs = SL * H > 64;
+    static constexpr int kLowRegs = 64;
+    static constexpr int kHighRegs = 216;
+    // TMEM columns per tcgen05.ld (two chunks in flight): narrower when the
+    // registers also hold 128 weights
+    static constexpr int kChunk = kSplitRegs ? 16 : 32;
+};
 
 // Position of the block `off` blocks after (pb, pj) in the CTA's walk order;
 // false if that is at or past the range end (eb, ej).
@@ -222,6 +248,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
     constexpr uint32_t kStageScaleBytes = KT * kSubScaleBytes;
     constexpr int EG = epi_groups_of(NN);
     constexpr uint32_t kEpiWarps = 4 * EG;
+    constexpr bool kCallWait = !EpiPlan<H, NN>::kSplitRegs;   // no calls with split registers
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -324,201 +351,208 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
     const uint32_t tmem_base = *tmem_slot;
     grid_dependency_wait();
 
-    if (producer) {
-        // ------------------------------------------------------------ producers
-        const int me = warp - 1;
-        const uint64_t policy = policy_evict_first();
-        int g = 0;                      // blocks consumed within the current chunk
-        uint32_t s = (uint32_t)me, ph = 0;
-        int qcount = 0, prev_b = -1, k = 0, my_issued = 0;
-        bool ok = true;
-        while (!w.done()) {
-            const bool mine = (k % kProducers) == me;
-            StageDesc sd;
-            sd.end = 0;
-            // lane l (< 2*KT) copies block slot l of the stage: sub-tile l/2, block l%2
-            int sphys[4] = {0, 0, 0, 0};
-            unsigned smask = 0;
-#pragma unroll
-            for (int i = 0; i < KT; ++i) {
-                sd.sub[i].cnt = 0;
-                sd.sub[i].flags = 0;
-                if (!ok || w.done()) continue;
-                const int c = w.cnt();
-                int flags = 0;
-                if (w.b != prev_b) {
-                    const int slot = qcount & 1;
-                    if (mine) {
-                        if (lane == 0) {
-                            ok = mbar_wait(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1,
-                                           abort_flag, a.status);
-                            if (ok) {
-                                const uint32_t qfb = qfull_bar0 + 8u * slot;
-                                mbar_arrive_expect_tx(qfb,
-                                                      (uint32_t)a.q_box_rows * kHeadDim + NH * 4u);
-                                tma_load_2d(q_base + slot * L.q_bytes, &qmap, qfb, 0, w.b * NH);
-                                bulk_load(base + L.w + slot * L.w_bytes,
-                                          a.weights + (long long)w.b * NH, NH * 4u, qfb);
-                            }
-                        }
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                    }
-                    flags |= kTileFirst;
-                    ++qcount;
-                    prev_b = w.b;
-                }
-                flags |= ((qcount - 1) & 1) << 4;
-                if (w.last_of_request(c)) flags |= kTileLast;
-                const int l0 = g, l1 = g + 1;
-                const int v0 = __shfl_sync(0xffffffffu, phys_cur, l0 & 31);
-                const int v0n = __shfl_sync(0xffffffffu, phys_nxt, l0 & 31);
-                const int v1 = __shfl_sync(0xffffffffu, phys_cur, l1 & 31);
-                const int v1n = __shfl_sync(0xffffffffu, phys_nxt, l1 & 31);
-                const int p0 = l0 < 32 ? v0 : v0n;
-                const int p1 = l1 < 32 ? v1 : v1n;
-                g += c;
-                if (g >= 32) {
-                    g -= 32;
-                    phys_cur = phys_nxt;
-                    phys_nxt = load_chunk();
-                }
-                if ((long long)w.j * kBlockKeys < a.max_context) {
-                    sphys[2 * i] = p0;
-                    smask |= 1u << (2 * i);
-                }
-                if (c == 2 && (long long)(w.j + 1) * kBlockKeys < a.max_context) {
-                    sphys[2 * i + 1] = p1;
-                    smask |= 1u << (2 * i + 1);
-                }
-                sd.sub[i].b = w.b;
-                sd.sub[i].j = w.j;
-                sd.sub[i].cnt = c;
-                sd.sub[i].len = min(w.len, a.max_context);
-                sd.sub[i].flags = flags;
-                w.advance(c);
-            }
-            if (!ok) break;
-            if (mine) {
-                if (lane == 0) ok = mbar_wait(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                if (lane == 0) {
-                    descs[s] = sd;
-                    mbar_arrive_expect_tx(full_bar0 + 8u * s,
-                                          (uint32_t)__popc(smask) * kFp8BlockBytes);
-                }
-                __syncwarp();
-                if (lane < 2 * KT && ((smask >> lane) & 1u)) {
-                    int pb = lane == 0 ? sphys[0] : lane == 1 ? sphys[1] : lane == 2 ? sphys[2] : sphys[3];
-                    const int bs = lane;
-                    if (pb < 0 || (long long)pb >= a.num_blocks) {
-                        atomicOr(a.status, kStatusBadBlock);
-                        pb = 0;
-                    }
-                    tma_load_3d_stream(k_base + s * kStageKeyBytes + bs * kFp8BlockKeyBytes, &kmap,
-                                       full_bar0 + 8u * s, 0, 0, pb, policy);
-                    bulk_load_stream(s_base + s * kStageScaleBytes + bs * (kBlockKeys * 4),
-                                     a.kv_fused + (long long)pb * kFp8BlockBytes + kFp8BlockKeyBytes,
-                                     kBlockKeys * 4, full_bar0 + 8u * s, policy);
-                }
-                ++my_issued;
-                s += kProducers;
-                if (s >= (uint32_t)S) { s -= S; ph ^= 1; }
-            }
-            ++k;
-        }
-        if (ok && (k % kProducers) == me && lane == 0) {
-            // end marker for the MMA and epilogue warps, in the stage after the last one
-            ok = mbar_wait(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
-            if (ok) {
-                descs[s].end = 1;
-                mbar_arrive(full_bar0 + 8u * s);
-            }
-        }
-        if (!ok && lane == 0) {
-            // drain: let every copy this warp issued land before the CTA exits
-            uint32_t ds = s, dph = ph;
-            for (int t = 0; t < my_issued && t < S / kProducers; ++t) {
-                if (ds < (uint32_t)kProducers) { ds += S; dph ^= 1; }
-                ds -= kProducers;
-                mbar_wait_drain(full_bar0 + 8u * ds, dph);
-            }
-            for (int qc = (qcount > 2 ? qcount - 2 : 0); qc < qcount; ++qc)
-                mbar_wait_drain(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
-        }
-    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
-        // ------------------------------------------------------------ MMA issuers
-        // MMA warp m issues sub-tile m of every stage (one tcgen05.mma takes a
-        // thread more cycles to issue than the tensor pipe needs to run it at
-        // these N, so two issuers run in parallel when a stage has two).
-        const int mw = warp == kMmaWarp ? 0 : 1;
-        if (lane == 0 && mw < KT) {
-            constexpr uint32_t idesc = make_idesc(0, 0, kTileKeys, N);
-            uint32_t s = 0, ph = 0, acc = 0, aph = 0, last_acc = 0, last_ph = 0;
-            int qcount = 0, done = 0;
+    if (warp < kFirstEpiWarp) {
+        // warpgroup 0: MMA issue and producers
+        if constexpr (EpiPlan<H, NN>::kSplitRegs) regs_dec<EpiPlan<H, NN>::kLowRegs>();
+        if (producer) {
+            // ------------------------------------------------------------ producers
+            const int me = warp - 1;
+            const uint64_t policy = policy_evict_first();
+            int g = 0;                      // blocks consumed within the current chunk
+            uint32_t s = (uint32_t)me, ph = 0;
+            int qcount = 0, prev_b = -1, k = 0, my_issued = 0;
             bool ok = true;
-            while (true) {
-                ok = mbar_wait(full_bar0 + 8u * s, ph, abort_flag, a.status);
-                if (!ok) break;
-                const StageDesc& sd = descs[s];
-                if (sd.end) break;
-                ok = mbar_wait(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
-                if (!ok) break;
-                // q / weights of every request that starts in this stage, in order
+            while (!w.done()) {
+                const bool mine = (k % kProducers) == me;
+                StageDesc sd;
+                sd.end = 0;
+                // lane l (< 2*KT) copies block slot l of the stage: sub-tile l/2, block l%2
+                int sphys[4] = {0, 0, 0, 0};
+                unsigned smask = 0;
 #pragma unroll
                 for (int i = 0; i < KT; ++i) {
-                    if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
-                        ok = mbar_wait(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
-                                       (qcount >> 1) & 1, abort_flag, a.status);
+                    sd.sub[i].cnt = 0;
+                    sd.sub[i].flags = 0;
+                    if (!ok || w.done()) continue;
+                    const int c = w.cnt();
+                    int flags = 0;
+                    if (w.b != prev_b) {
+                        const int slot = qcount & 1;
+                        if (mine) {
+                            if (lane == 0) {
+                                ok = mbar_wait<kCallWait>(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1,
+                                               abort_flag, a.status);
+                                if (ok) {
+                                    const uint32_t qfb = qfull_bar0 + 8u * slot;
+                                    mbar_arrive_expect_tx(qfb,
+                                                          (uint32_t)a.q_box_rows * kHeadDim + NH * 4u);
+                                    tma_load_2d(q_base + slot * L.q_bytes, &qmap, qfb, 0, w.b * NH);
+                                    bulk_load(base + L.w + slot * L.w_bytes,
+                                              a.weights + (long long)w.b * NH, NH * 4u, qfb);
+                                }
+                            }
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                        }
+                        flags |= kTileFirst;
                         ++qcount;
+                        prev_b = w.b;
                     }
+                    flags |= ((qcount - 1) & 1) << 4;
+                    if (w.last_of_request(c)) flags |= kTileLast;
+                    const int l0 = g, l1 = g + 1;
+                    const int v0 = __shfl_sync(0xffffffffu, phys_cur, l0 & 31);
+                    const int v0n = __shfl_sync(0xffffffffu, phys_nxt, l0 & 31);
+                    const int v1 = __shfl_sync(0xffffffffu, phys_cur, l1 & 31);
+                    const int v1n = __shfl_sync(0xffffffffu, phys_nxt, l1 & 31);
+                    const int p0 = l0 < 32 ? v0 : v0n;
+                    const int p1 = l1 < 32 ? v1 : v1n;
+                    g += c;
+                    if (g >= 32) {
+                        g -= 32;
+                        phys_cur = phys_nxt;
+                        phys_nxt = load_chunk();
+                    }
+                    if ((long long)w.j * kBlockKeys < a.max_context) {
+                        sphys[2 * i] = p0;
+                        smask |= 1u << (2 * i);
+                    }
+                    if (c == 2 && (long long)(w.j + 1) * kBlockKeys < a.max_context) {
+                        sphys[2 * i + 1] = p1;
+                        smask |= 1u << (2 * i + 1);
+                    }
+                    sd.sub[i].b = w.b;
+                    sd.sub[i].j = w.j;
+                    sd.sub[i].cnt = c;
+                    sd.sub[i].len = min(w.len, a.max_context);
+                    sd.sub[i].flags = flags;
+                    w.advance(c);
                 }
                 if (!ok) break;
-                tc_fence_after();
-                const int cnt = sd.sub[mw].cnt;
-                if (cnt != 0) {
-                    const int slot = (sd.sub[mw].flags >> 4) & 1;
-                    const uint64_t ad =
-                        smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
-                    const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
-                    const uint32_t dt = tmem_base + acc * COLS + mw * N;
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 32; ++kk)
-                        mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
-                    mma_commit(tfull_bar0 + 8u * acc);
-                    last_acc = acc;
-                    last_ph = aph;
-                    ++done;
-                } else {
-                    mbar_arrive(tfull_bar0 + 8u * acc);   // nothing issued for this sub-tile
+                if (mine) {
+                    if (lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        descs[s] = sd;
+                        mbar_arrive_expect_tx(full_bar0 + 8u * s,
+                                              (uint32_t)__popc(smask) * kFp8BlockBytes);
+                    }
+                    __syncwarp();
+                    if (lane < 2 * KT && ((smask >> lane) & 1u)) {
+                        int pb = lane == 0 ? sphys[0] : lane == 1 ? sphys[1] : lane == 2 ? sphys[2] : sphys[3];
+                        const int bs = lane;
+                        if (pb < 0 || (long long)pb >= a.num_blocks) {
+                            atomicOr(a.status, kStatusBadBlock);
+                            pb = 0;
+                        }
+                        tma_load_3d_stream(k_base + s * kStageKeyBytes + bs * kFp8BlockKeyBytes, &kmap,
+                                           full_bar0 + 8u * s, 0, 0, pb, policy);
+                        bulk_load_stream(s_base + s * kStageScaleBytes + bs * (kBlockKeys * 4),
+                                         a.kv_fused + (long long)pb * kFp8BlockBytes + kFp8BlockKeyBytes,
+                                         kBlockKeys * 4, full_bar0 + 8u * s, policy);
+                    }
+                    ++my_issued;
+                    s += kProducers;
+                    if (s >= (uint32_t)S) { s -= S; ph ^= 1; }
                 }
-                if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
-                if (++acc == NACC) { acc = 0; aph ^= 1; }
+                ++k;
             }
-            if (done > 0) {
-                // every MMA this warp issued has completed before TMEM is
-                // released: the phase of its last commit completes only then
-                mbar_wait_drain(tfull_bar0 + 8u * last_acc, last_ph);
+            if (ok && (k % kProducers) == me && lane == 0) {
+                // end marker for the MMA and epilogue warps, in the stage after the last one
+                ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+                if (ok) {
+                    descs[s].end = 1;
+                    mbar_arrive(full_bar0 + 8u * s);
+                }
+            }
+            if (!ok && lane == 0) {
+                // drain: let every copy this warp issued land before the CTA exits
+                uint32_t ds = s, dph = ph;
+                for (int t = 0; t < my_issued && t < S / kProducers; ++t) {
+                    if (ds < (uint32_t)kProducers) { ds += S; dph ^= 1; }
+                    ds -= kProducers;
+                    mbar_wait_drain<kCallWait>(full_bar0 + 8u * ds, dph);
+                }
+                for (int qc = (qcount > 2 ? qcount - 2 : 0); qc < qcount; ++qc)
+                    mbar_wait_drain<kCallWait>(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
+            }
+        } else {
+            // ------------------------------------------------------------ MMA issuers
+            // MMA warp m issues sub-tile m of every stage (one tcgen05.mma takes a
+            // thread more cycles to issue than the tensor pipe needs to run it at
+            // these N, so two issuers run in parallel when a stage has two).
+            const int mw = warp == kMmaWarp ? 0 : 1;
+            if (lane == 0 && mw < KT) {
+                constexpr uint32_t idesc = make_idesc(0, 0, kTileKeys, N);
+                uint32_t s = 0, ph = 0, acc = 0, aph = 0, last_acc = 0, last_ph = 0;
+                int qcount = 0, done = 0;
+                bool ok = true;
+                while (true) {
+                    ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
+                    if (!ok) break;
+                    const StageDesc& sd = descs[s];
+                    if (sd.end) break;
+                    ok = mbar_wait<kCallWait>(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
+                    if (!ok) break;
+                    // q / weights of every request that starts in this stage, in order
+#pragma unroll
+                    for (int i = 0; i < KT; ++i) {
+                        if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
+                            ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
+                                           (qcount >> 1) & 1, abort_flag, a.status);
+                            ++qcount;
+                        }
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int cnt = sd.sub[mw].cnt;
+                    if (cnt != 0) {
+                        const int slot = (sd.sub[mw].flags >> 4) & 1;
+                        const uint64_t ad =
+                            smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
+                        const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
+                        const uint32_t dt = tmem_base + acc * COLS + mw * N;
+#pragma unroll
+                        for (int kk = 0; kk < kHeadDim / 32; ++kk)
+                            mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                        mma_commit(tfull_bar0 + 8u * acc);
+                        last_acc = acc;
+                        last_ph = aph;
+                        ++done;
+                    } else {
+                        mbar_arrive(tfull_bar0 + 8u * acc);   // nothing issued for this sub-tile
+                    }
+                    if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
+                    if (++acc == NACC) { acc = 0; aph ^= 1; }
+                }
+                if (done > 0) {
+                    // every MMA this warp issued has completed before TMEM is
+                    // released: the phase of its last commit completes only then
+                    mbar_wait_drain<kCallWait>(tfull_bar0 + 8u * last_acc, last_ph);
+                }
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        if constexpr (EpiPlan<H, NN>::kSplitRegs) regs_inc<EpiPlan<H, NN>::kHighRegs>();
         const int grp = (warp - kFirstEpiWarp) >> 2;
         const int quad = warp & 3;             // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;      // key row within the sub-tile
         const int page = row >> 6;
         const int key = row & 63;
-        // groups per sub-tile; group g takes sub-tile g / GS and slots t = g % GS (mod GS)
-        constexpr int GS = EG / KT;
-        constexpr int SL = (NN + GS - 1) / GS;   // slots per warp
-        const int my_sub = grp / GS;
-        const int first_slot = grp % GS;
+        using E = EpiPlan<H, NN>;
+        // sub-tiles of each stage this group processes, and its slots
+        constexpr int NSUB = E::kSubSplit ? 1 : KT;
+        const int first_slot = E::kSubSplit ? 0 : grp;
+        const bool short_group = first_slot + (E::SL - 1) * E::GS >= NN;   // one slot fewer
+        uint64_t wp[E::kWeightPairs];
+        int cur_b = -1;                        // request whose weights wp holds
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         uint32_t s = 0, ph = 0, acc = 0, aph = 0;
         int qcount = 0;
         bool ok = true;
         while (true) {
-            ok = mbar_wait(full_bar0 + 8u * s, ph, abort_flag, a.status);
+            ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
             if (!ok) break;
             const StageDesc& sd = descs[s];
             if (sd.end) break;
@@ -527,35 +561,67 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
                 if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
-                    ok = mbar_wait(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
+                    ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
                                    (qcount >> 1) & 1, abort_flag, a.status);
                     ++qcount;
                 }
             }
             if (!ok) break;
-            ok = mbar_wait(tfull_bar0 + 8u * acc, aph, abort_flag, a.status);
+            ok = mbar_wait<kCallWait>(tfull_bar0 + 8u * acc, aph, abort_flag, a.status);
             if (!ok) break;
             tc_fence_after();
             // The MMAs of this stage are complete, so its key buffers are no
-            // longer read: take the descriptor fields and this key's scale
+            // longer read: take the descriptor fields and this key's scales
             // into registers and hand the stage back to the producers before
             // the arithmetic, which then overlaps with the next copies.
-            const SubDesc d = sd.sub[my_sub];
-            const float sp = scales_smem[s * (kStageScaleBytes / 4) + my_sub * kTileKeys + row];
+            SubDesc d[NSUB];
+            float sp[NSUB];
+#pragma unroll
+            for (int ii = 0; ii < NSUB; ++ii) {
+                const int i = E::kSubSplit ? grp : ii;
+                d[ii] = sd.sub[i];
+                sp[ii] = scales_smem[s * (kStageScaleBytes / 4) + i * kTileKeys + row];
+            }
             int rel0 = -1, rel1 = -1;
             if (sd.sub[0].cnt != 0 && (sd.sub[0].flags & kTileLast)) rel0 = (sd.sub[0].flags >> 4) & 1;
             if (KT == 2 && sd.sub[1].cnt != 0 && (sd.sub[1].flags & kTileLast))
                 rel1 = (sd.sub[1].flags >> 4) & 1;
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar0 + 8u * s);
-            if (d.cnt != 0) {
-                const int pos = (d.j + page) * kBlockKeys + key;
-                const bool valid = page < d.cnt && pos < d.len;
-                const float4* w4 = reinterpret_cast<const float4*>(
-                    smem + L.w + ((d.flags >> 4) & 1) * L.w_bytes);
-                float* orow = a.out + (long long)d.b * NN * a.out_stride + pos;
-                slot_logits<H, NN, SL, GS>(lane_addr + acc * COLS + my_sub * N, w4, first_slot,
-                                           sp, valid, orow, a.out_stride);
+#pragma unroll
+            for (int ii = 0; ii < NSUB; ++ii) {
+                const int i = E::kSubSplit ? grp : ii;
+                if (d[ii].cnt == 0) continue;
+                if (d[ii].b != cur_b) {
+                    // first sub-tile of a new request for this warp
+                    const float4* w4 = reinterpret_cast<const float4*>(
+                        smem + L.w + ((d[ii].flags >> 4) & 1) * L.w_bytes);
+#pragma unroll
+                    for (int k = 0; k < E::SL; ++k) {
+                        const int t = first_slot + k * E::GS;
+#pragma unroll
+                        for (int h = 0; h < H; h += 4) {
+                            const float4 v = t < NN ? w4[t * (H / 4) + h / 4]
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                            wp[(k * H + h) / 2] = pack2(v.x, v.y);
+                            wp[(k * H + h) / 2 + 1] = pack2(v.z, v.w);
+                        }
+                    }
+                    cur_b = d[ii].b;
+                }
+                const int pos = (d[ii].j + page) * kBlockKeys + key;
+                const bool valid = page < d[ii].cnt && pos < d[ii].len;
+                float* orow = a.out + (long long)d[ii].b * NN * a.out_stride + pos;
+                const uint32_t taddr = lane_addr + acc * COLS + i * N;
+                if constexpr (NN % E::GS != 0) {
+                    if (short_group) {
+                        slot_logits<H, E::SL - 1, E::GS, E::kChunk>(
+                            taddr, wp, first_slot, sp[ii], valid, orow, a.out_stride);
+                        continue;
+                    }
+                }
+                slot_logits<H, E::SL, E::GS, E::kChunk>(taddr, wp, first_slot, sp[ii], valid,
+                                                        orow, a.out_stride);
             }
             tc_fence_before();
             __syncwarp();
@@ -593,6 +659,18 @@ cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Ar
         e = cudaFuncSetAttribute(logits_kernel<H, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
+        if constexpr (EpiPlan<H, NN>::kSplitRegs) {
+            // the warpgroups' register budgets must fit the block's allocation,
+            // else the epilogue's setmaxnreg.inc would wait forever
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, logits_kernel<H, NN>);
+            if (e != cudaSuccess) return e;
+            const long long pool = (long long)fa.numRegs * threads_of(NN);
+            const long long need = 128LL * EpiPlan<H, NN>::kLowRegs +
+                                   128LL * epi_groups_of(NN) * EpiPlan<H, NN>::kHighRegs;
+            if (fa.numRegs > EpiPlan<H, NN>::kHighRegs || pool < need)
+                return cudaErrorInvalidConfiguration;
+        }
         configured_device = dev;
         configured_smem = smem;
     }

@@ -35,6 +35,22 @@ __device__ __forceinline__ void allow_dependent_launch()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the
+// same call).  dec hands registers back to the CTA's pool; inc takes them from
+// it and waits until the pool holds enough, so the budgets of all warpgroups
+// must add up to no more than the block was launched with (checked on the
+// host before every launch that uses them).
+template <int R>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Waits until every grid this one depends on has completed and its memory
 // operations are visible.  Must precede any global read of inputs or write of
 // outputs.  A no-op when the kernel was launched without the attribute.
@@ -84,16 +100,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Same, but a thread whose phase is not yet complete may be suspended in
+// hardware for up to suspend_ns (it resumes as soon as the phase completes),
+// so a waiting warp takes no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t suspend_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Slow path of mbar_wait: spin for at most kWaitLimitNs.  Gives up early
 // (returning false) once *abort is set by another role of the CTA.  On
 // timeout, records kStatusWaitTimeout in *status, raises *abort and returns
 // false.  Never spins forever.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
-                                            unsigned int* status)
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status)
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
         if ((it & 31u) == 0) {
             if (abort != nullptr && *abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -105,19 +138,31 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
 }
 
+// The slow path out of line, which keeps the loops around the waits short.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, unsigned int* status)
+{
+    return mbar_spin(bar, parity, abort, status);
+}
+
 // Wait for the phase with the given parity to complete (bounded, see above).
+// kCall = false inlines the slow path too: a kernel that re-splits its
+// registers between warpgroups (setmaxnreg) must contain no calls.
+template <bool kCall = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort, status);
+    if constexpr (kCall) return mbar_wait_slow(bar, parity, abort, status);
+    else return mbar_spin(bar, parity, abort, status);
 }
 
 // Same, ignoring the abort flag: used while draining copies already in flight
 // before the CTA exits.
+template <bool kCall = true>
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity)
 {
-    return mbar_wait(bar, parity, nullptr, nullptr);
+    return mbar_wait<kCall>(bar, parity, nullptr, nullptr);
 }
 
 // ------------------------------------------------------------------ TMA
