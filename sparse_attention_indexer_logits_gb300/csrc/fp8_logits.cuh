@@ -55,7 +55,7 @@ namespace fp8 {
 constexpr int kSubKeyBytes = kTileKeys * kHeadDim;     // 16 KB: one sub-tile of keys
 constexpr int kSubScaleBytes = kTileKeys * 4;          // 512 B
 constexpr int kMmaWarp = 0;                            // also allocates TMEM
-constexpr int kProducers = 2;                          // warps 1 and 2, alternate stages
+constexpr int kProducerWarp = 1;                       // warp 2 has no role
 constexpr int kMmaWarp2 = 3;                           // issues sub-tile 1 of each stage
 constexpr int kFirstEpiWarp = 4;
 // Two epilogue warpgroups: one per sub-tile when a stage holds two, else
@@ -194,8 +194,8 @@ __device__ __forceinline__ void slot_logits(uint32_t taddr0, const uint64_t (&wp
 // can.  Only with next_n*H > 128 at one sub-tile per stage (H = 64,
 // next_n >= 3) are there 128; then the CTA's registers are re-split, the
 // MMA/producer warpgroup dropping to kLowRegs so that the two epilogue
-// warpgroups can hold kHighRegs each (128 x 64 + 256 x 216 = 63488, within
-// the 384 x 168 registers of the block).  ptxas allocates each warpgroup's
+// warpgroups can hold kHighRegs each (128 x 88 + 256 x 208 = 64512, the
+// 384 x 168 registers of the block).  ptxas allocates each warpgroup's
 // branch within its budget only if no call (a non-inlined function) sits in
 // it, which is why the waits are fully inlined.
 template <int H, int NN>
@@ -206,32 +206,105 @@ struct EpiPlan {
     static constexpr int SL = (NN + GS - 1) / GS;           // slots of group 0
     static constexpr int kWeightPairs = SL * H / 2;
     static constexpr bool kSplitRegs = SL * H > 64;
-    static constexpr int kLowRegs = 64;
-    static constexpr int kHighRegs = 216;
+    static constexpr int kLowRegs = 88;
+    static constexpr int kHighRegs = 208;
     // TMEM columns per tcgen05.ld (two chunks in flight): narrower when the
     // registers also hold 128 weights
     static constexpr int kChunk = kSplitRegs ? 16 : 32;
 };
 
-// Position of the block `off` blocks after (pb, pj) in the CTA's walk order;
-// false if that is at or past the range end (eb, ej).
-__device__ __forceinline__ bool block_at(const int32_t* __restrict__ lens, int batch, int pb,
-                                         int pj, int pnb, int eb, int ej, int off, int& ob,
-                                         int& oj)
+// Producer window: up to 32 consecutive sub-tiles of the CTA's range, one per
+// lane, built by the whole warp at once.  Within the range, request b's
+// sub-tiles pair its blocks from j0(b) (sj for the first request, else 0):
+// (j0, j0+1), (j0+2, j0+3), ..., the last one single if the request's part of
+// the range has an odd number of blocks.  A window starts at a sub-tile
+// boundary (cb, cj) and holds a whole number of stages unless it is the last.
+struct Window {
+    int b, j, cnt, len;    // this lane's sub-tile (lanes < n)
+    bool first, last;      // first / last sub-tile of request b in the range
+    bool ld0, ld1;         // which of its two blocks lie below max_context
+    int phys0, phys1;      // their physical blocks (read from block_table)
+    int n;                 // sub-tiles in the window
+    int nb, nj;            // where the next window starts; nb < 0: nothing left
+    unsigned first_mask;   // lanes holding a first sub-tile
+};
+
+// Number of lanes r whose inclusive prefix p_r is <= v (p non-decreasing over
+// the lanes): the lane index whose range of sub-tiles contains sub-tile v.
+__device__ __forceinline__ int warp_locate(int p, int v)
 {
-    int b = pb, j = pj + off, nb = pnb;
-    while (true) {
-        if (b >= batch) return false;
-        if (j < nb) break;
-        j -= nb;
-        do {
-            ++b;
-        } while (b < batch && (nb = blocks_of(__ldg(lens + b))) == 0);
+    int pos = 0;
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        const int t = __shfl_sync(0xffffffffu, p, pos + k - 1);
+        if (t <= v) pos += k;
     }
-    if (b > eb || (b == eb && j >= ej)) return false;
-    ob = b;
-    oj = j;
-    return true;
+    return pos;
+}
+
+template <int KT>
+__device__ __forceinline__ Window make_window(const Fp8Args& a, int cb, int cj, int sb, int sj,
+                                              int eb, int ej, int lane)
+{
+    Window w;
+    // lane r describes request cb + r: its blocks in the range from this
+    // window's start, and the sub-tiles they make
+    const int rq = cb + lane;
+    const bool in_rng = rq < a.batch && rq <= eb;
+    const int len_r = in_rng ? __ldg(a.seq_lens + rq) : 0;
+    const int nb_r = blocks_of(len_r);
+    const int lim_r = rq == eb ? ej : nb_r;               // end of the request's part of the range
+    const int blk_r = in_rng ? max(0, lim_r - (lane == 0 ? cj : 0)) : 0;
+    const int st_r = (blk_r + 1) >> 1;
+    int p = st_r;                                         // inclusive prefix over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, p, o);
+        if (lane >= o) p += t;
+    }
+    const int total = __shfl_sync(0xffffffffu, p, 31);
+    // lane l takes sub-tile l
+    const int r = warp_locate(p, lane);
+    const int p_r = __shfl_sync(0xffffffffu, p, r);
+    const int s_r = __shfl_sync(0xffffffffu, st_r, r);
+    const int l_r = __shfl_sync(0xffffffffu, lim_r, r);
+    const int n_r = __shfl_sync(0xffffffffu, len_r, r);
+    w.b = cb + r;
+    w.j = (r == 0 ? cj : 0) + 2 * (lane - (p_r - s_r));
+    w.cnt = min(2, l_r - w.j);
+    w.len = min(n_r, a.max_context);
+    w.first = w.j == (w.b == sb ? sj : 0);
+    w.last = w.j + w.cnt == l_r;
+    // extent of the window and the start of the next one
+    const bool beyond = cb + 32 <= eb && cb + 32 < a.batch;   // requests not yet looked at
+    w.n = min(total, 32);
+    if (total > 32) {
+        const int r32 = warp_locate(p, 32);
+        const int p32 = __shfl_sync(0xffffffffu, p, r32);
+        const int s32 = __shfl_sync(0xffffffffu, st_r, r32);
+        w.nb = cb + r32;
+        w.nj = (r32 == 0 ? cj : 0) + 2 * (32 - (p32 - s32));
+    } else if (beyond) {
+        w.nb = cb + 32;
+        w.nj = 0;
+    } else {
+        w.nb = -1;
+        w.nj = 0;
+    }
+    if (KT == 2 && w.nb >= 0 && (w.n & 1)) {
+        // keep whole stages: the odd sub-tile opens the next window
+        --w.n;
+        w.nb = __shfl_sync(0xffffffffu, w.b, w.n);
+        w.nj = __shfl_sync(0xffffffffu, w.j, w.n);
+    }
+    const bool mine = lane < w.n;
+    w.first_mask = __ballot_sync(0xffffffffu, mine && w.first);
+    w.ld0 = mine && (long long)w.j * kBlockKeys < a.max_context;
+    w.ld1 = mine && w.cnt == 2 && (long long)(w.j + 1) * kBlockKeys < a.max_context;
+    const int32_t* row = a.block_table + (long long)w.b * a.bt_stride + w.j;
+    w.phys0 = w.ld0 ? __ldg(row) : 0;
+    w.phys1 = w.ld1 ? __ldg(row + 1) : 0;
+    return w;
 }
 
 template <int H, int NN>
@@ -279,33 +352,12 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
     // The next call may be placed on SMs as this grid leaves them; nothing
     // here touches global memory before grid_dependency_wait.
     allow_dependent_launch();
-    const bool producer = warp >= 1 && warp <= kProducers;
-    // Producer state.  The producers compute their range and issue the first
-    // block-table loads before the CTA-wide barrier, so that these global
-    // round trips overlap the TMEM allocation and the barrier set-up.
+    const bool producer = warp == kProducerWarp;
+    // The producer computes its range and its first window (block-table
+    // reads included) before the CTA-wide barrier, so that these global round
+    // trips overlap the TMEM allocation and the barrier set-up.
     int sb = 0, sj = 0, eb = 0, ej = 0;
-    Walk w;
-    // block-table chunks: lane l of chunk k holds the physical block of the
-    // CTA's (32k + l)-th block (-1 past the range or past max_context)
-    int cb = 0, cj = 0, cnb = 0;
-    bool chunks_left = false;
-    auto load_chunk = [&]() -> int {
-        int phys = -1;
-        if (chunks_left) {
-            int ob, oj;
-            if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, lane, ob, oj) &&
-                (long long)oj * kBlockKeys < a.max_context)
-                phys = __ldg(a.block_table + (long long)ob * a.bt_stride + oj);
-            int nb_, nj_;
-            if (block_at(a.seq_lens, a.batch, cb, cj, cnb, eb, ej, 32, nb_, nj_)) {
-                cb = nb_; cj = nj_; cnb = blocks_of(__ldg(a.seq_lens + cb));
-            } else {
-                chunks_left = false;
-            }
-        }
-        return phys;
-    };
-    int phys_cur = -1, phys_nxt = -1;
+    Window win;
     if (producer) {
         grid_dependency_wait();
         if (a.schedule_meta != nullptr) {
@@ -319,11 +371,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             const long long s1 = range_start(total, gridDim.x, blockIdx.x + 1);
             warp_locate2(a.seq_lens, a.batch, s0, s1, sb, sj, eb, ej);
         }
-        w.init(a.seq_lens, a.batch, sb, sj, eb, ej);
-        cb = sb; cj = sj; cnb = w.nbb;
-        chunks_left = !w.done();
-        phys_cur = load_chunk();
-        phys_nxt = load_chunk();
+        win = make_window<KT>(a, sb, sj, sb, sj, eb, ej, lane);
     } else if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), tmem_cols_of(N));
         tmem_relinquish();
@@ -355,109 +403,102 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
         // warpgroup 0: MMA issue and producers
         if constexpr (EpiPlan<H, NN>::kSplitRegs) regs_dec<EpiPlan<H, NN>::kLowRegs>();
         if (producer) {
-            // ------------------------------------------------------------ producers
-            const int me = warp - 1;
+            // ------------------------------------------------------------ producer
             const uint64_t policy = policy_evict_first();
-            int g = 0;                      // blocks consumed within the current chunk
-            uint32_t s = (uint32_t)me, ph = 0;
-            int qcount = 0, prev_b = -1, k = 0, my_issued = 0;
+            uint32_t s = 0, ph = 0;
+            int qbase = 0;                  // requests started in earlier windows
+            int issued = 0, q_issued = 0;   // stages published, q tiles requested
             bool ok = true;
-            while (!w.done()) {
-                const bool mine = (k % kProducers) == me;
-                StageDesc sd;
-                sd.end = 0;
-                // lane l (< 2*KT) copies block slot l of the stage: sub-tile l/2, block l%2
-                int sphys[4] = {0, 0, 0, 0};
-                unsigned smask = 0;
+            // TMA of one block's keys (8 KB, 128-byte swizzle) and bulk copy of
+            // its 64 scales into stage s
+            auto load_block = [&](uint32_t kdst, uint32_t sdst, int pb) {
+                if (pb < 0 || (long long)pb >= a.num_blocks) {
+                    atomicOr(a.status, kStatusBadBlock);
+                    pb = 0;
+                }
+                tma_load_3d_stream(kdst, &kmap, full_bar0 + 8u * s, 0, 0, pb, policy);
+                bulk_load_stream(sdst, a.kv_fused + (long long)pb * kFp8BlockBytes + kFp8BlockKeyBytes,
+                                 kBlockKeys * 4, full_bar0 + 8u * s, policy);
+            };
+            while (true) {
+                Window nxt;
+                bool have_nxt = false;
+                const int stages_here = (win.n + KT - 1) / KT;
+                // q index of this lane's request: requests started before it
+                const int qidx = qbase + __popc(win.first_mask & ((2u << lane) - 1u)) - 1;
+                for (int st = 0; st < stages_here; ++st) {
+                    const int o0 = st * KT;
+                    const int i = lane - o0;                 // sub-tile slot this lane fills
+                    const bool own = i >= 0 && i < KT && lane < win.n;
+                    // q / weights of each request starting in this stage, in order
 #pragma unroll
-                for (int i = 0; i < KT; ++i) {
-                    sd.sub[i].cnt = 0;
-                    sd.sub[i].flags = 0;
-                    if (!ok || w.done()) continue;
-                    const int c = w.cnt();
-                    int flags = 0;
-                    if (w.b != prev_b) {
-                        const int slot = qcount & 1;
-                        if (mine) {
-                            if (lane == 0) {
-                                ok = mbar_wait<kCallWait>(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1,
-                                               abort_flag, a.status);
+                    for (int k = 0; k < KT; ++k) {
+                        const int ol = o0 + k;
+                        if (ol < win.n && ((win.first_mask >> ol) & 1u)) {
+                            if (lane == ol) {
+                                const int slot = qidx & 1;
+                                ok = mbar_wait<kCallWait>(qempty_bar0 + 8u * slot,
+                                                          ((qidx >> 1) & 1) ^ 1, abort_flag, a.status);
                                 if (ok) {
                                     const uint32_t qfb = qfull_bar0 + 8u * slot;
                                     mbar_arrive_expect_tx(qfb,
                                                           (uint32_t)a.q_box_rows * kHeadDim + NH * 4u);
-                                    tma_load_2d(q_base + slot * L.q_bytes, &qmap, qfb, 0, w.b * NH);
+                                    tma_load_2d(q_base + slot * L.q_bytes, &qmap, qfb, 0, win.b * NH);
                                     bulk_load(base + L.w + slot * L.w_bytes,
-                                              a.weights + (long long)w.b * NH, NH * 4u, qfb);
+                                              a.weights + (long long)win.b * NH, NH * 4u, qfb);
                                 }
                             }
-                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            ok = __shfl_sync(0xffffffffu, ok, ol);
+                            if (!ok) break;
+                            ++q_issued;
                         }
-                        flags |= kTileFirst;
-                        ++qcount;
-                        prev_b = w.b;
                     }
-                    flags |= ((qcount - 1) & 1) << 4;
-                    if (w.last_of_request(c)) flags |= kTileLast;
-                    const int l0 = g, l1 = g + 1;
-                    const int v0 = __shfl_sync(0xffffffffu, phys_cur, l0 & 31);
-                    const int v0n = __shfl_sync(0xffffffffu, phys_nxt, l0 & 31);
-                    const int v1 = __shfl_sync(0xffffffffu, phys_cur, l1 & 31);
-                    const int v1n = __shfl_sync(0xffffffffu, phys_nxt, l1 & 31);
-                    const int p0 = l0 < 32 ? v0 : v0n;
-                    const int p1 = l1 < 32 ? v1 : v1n;
-                    g += c;
-                    if (g >= 32) {
-                        g -= 32;
-                        phys_cur = phys_nxt;
-                        phys_nxt = load_chunk();
-                    }
-                    if ((long long)w.j * kBlockKeys < a.max_context) {
-                        sphys[2 * i] = p0;
-                        smask |= 1u << (2 * i);
-                    }
-                    if (c == 2 && (long long)(w.j + 1) * kBlockKeys < a.max_context) {
-                        sphys[2 * i + 1] = p1;
-                        smask |= 1u << (2 * i + 1);
-                    }
-                    sd.sub[i].b = w.b;
-                    sd.sub[i].j = w.j;
-                    sd.sub[i].cnt = c;
-                    sd.sub[i].len = min(w.len, a.max_context);
-                    sd.sub[i].flags = flags;
-                    w.advance(c);
-                }
-                if (!ok) break;
-                if (mine) {
+                    if (!ok) break;
                     if (lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
+                    // publish the stage: each owner lane its sub-tile, lane 0 the rest
+                    StageDesc& sd = descs[s];
+                    if (own) {
+                        SubDesc& d = sd.sub[i];
+                        d.b = win.b;
+                        d.j = win.j;
+                        d.cnt = win.cnt;
+                        d.len = win.len;
+                        d.flags = (win.first ? kTileFirst : 0) | (win.last ? kTileLast : 0) |
+                                  ((qidx & 1) << 4);
+                    }
                     if (lane == 0) {
-                        descs[s] = sd;
-                        mbar_arrive_expect_tx(full_bar0 + 8u * s,
-                                              (uint32_t)__popc(smask) * kFp8BlockBytes);
+                        for (int k = win.n - o0; k < KT; ++k) sd.sub[k].cnt = 0;
+                        sd.end = 0;
                     }
+                    const unsigned m0 = __ballot_sync(0xffffffffu, own && win.ld0);
+                    const unsigned m1 = __ballot_sync(0xffffffffu, own && win.ld1);
                     __syncwarp();
-                    if (lane < 2 * KT && ((smask >> lane) & 1u)) {
-                        int pb = lane == 0 ? sphys[0] : lane == 1 ? sphys[1] : lane == 2 ? sphys[2] : sphys[3];
-                        const int bs = lane;
-                        if (pb < 0 || (long long)pb >= a.num_blocks) {
-                            atomicOr(a.status, kStatusBadBlock);
-                            pb = 0;
-                        }
-                        tma_load_3d_stream(k_base + s * kStageKeyBytes + bs * kFp8BlockKeyBytes, &kmap,
-                                           full_bar0 + 8u * s, 0, 0, pb, policy);
-                        bulk_load_stream(s_base + s * kStageScaleBytes + bs * (kBlockKeys * 4),
-                                         a.kv_fused + (long long)pb * kFp8BlockBytes + kFp8BlockKeyBytes,
-                                         kBlockKeys * 4, full_bar0 + 8u * s, policy);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(full_bar0 + 8u * s,
+                                              (uint32_t)(__popc(m0) + __popc(m1)) * kFp8BlockBytes);
+                    __syncwarp();
+                    if (own) {
+                        const uint32_t kdst = k_base + s * kStageKeyBytes + (uint32_t)i * kSubKeyBytes;
+                        const uint32_t sdst = s_base + s * kStageScaleBytes + (uint32_t)i * kSubScaleBytes;
+                        if (win.ld0) load_block(kdst, sdst, win.phys0);
+                        if (win.ld1) load_block(kdst + kFp8BlockKeyBytes, sdst + kBlockKeys * 4, win.phys1);
                     }
-                    ++my_issued;
-                    s += kProducers;
-                    if (s >= (uint32_t)S) { s -= S; ph ^= 1; }
+                    ++issued;
+                    if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
+                    if (st == 0 && win.nb >= 0) {
+                        // the next window's block-table reads overlap this window's stages
+                        nxt = make_window<KT>(a, win.nb, win.nj, sb, sj, eb, ej, lane);
+                        have_nxt = true;
+                    }
                 }
-                ++k;
+                if (!ok || win.nb < 0) break;
+                qbase += __popc(win.first_mask);
+                if (!have_nxt) nxt = make_window<KT>(a, win.nb, win.nj, sb, sj, eb, ej, lane);
+                win = nxt;
             }
-            if (ok && (k % kProducers) == me && lane == 0) {
+            if (ok && lane == 0) {
                 // end marker for the MMA and epilogue warps, in the stage after the last one
                 ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
                 if (ok) {
@@ -468,21 +509,24 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             if (!ok && lane == 0) {
                 // drain: let every copy this warp issued land before the CTA exits
                 uint32_t ds = s, dph = ph;
-                for (int t = 0; t < my_issued && t < S / kProducers; ++t) {
-                    if (ds < (uint32_t)kProducers) { ds += S; dph ^= 1; }
-                    ds -= kProducers;
+                for (int t = 0; t < issued && t < S; ++t) {
+                    if (ds == 0) { ds = S; dph ^= 1; }
+                    --ds;
                     mbar_wait_drain<kCallWait>(full_bar0 + 8u * ds, dph);
                 }
-                for (int qc = (qcount > 2 ? qcount - 2 : 0); qc < qcount; ++qc)
+                for (int qc = (q_issued > 2 ? q_issued - 2 : 0); qc < q_issued; ++qc)
                     mbar_wait_drain<kCallWait>(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
             }
-        } else {
+        } else if (warp == kMmaWarp || warp == kMmaWarp2) {
             // ------------------------------------------------------------ MMA issuers
             // MMA warp m issues sub-tile m of every stage (one tcgen05.mma takes a
             // thread more cycles to issue than the tensor pipe needs to run it at
-            // these N, so two issuers run in parallel when a stage has two).
+            // these N, so two issuers run in parallel when a stage has two).  The
+            // whole warp runs the loop and lane 0 issues: a warp kept converged
+            // is scheduled promptly, where one whose other lanes wait at the
+            // CTA barrier is not.
             const int mw = warp == kMmaWarp ? 0 : 1;
-            if (lane == 0 && mw < KT) {
+            if (mw < KT) {
                 constexpr uint32_t idesc = make_idesc(0, 0, kTileKeys, N);
                 uint32_t s = 0, ph = 0, acc = 0, aph = 0, last_acc = 0, last_ph = 0;
                 int qcount = 0, done = 0;
@@ -507,21 +551,24 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                     tc_fence_after();
                     const int cnt = sd.sub[mw].cnt;
                     if (cnt != 0) {
-                        const int slot = (sd.sub[mw].flags >> 4) & 1;
-                        const uint64_t ad =
-                            smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
-                        const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
-                        const uint32_t dt = tmem_base + acc * COLS + mw * N;
+                        if (lane == 0) {
+                            const int slot = (sd.sub[mw].flags >> 4) & 1;
+                            const uint64_t ad =
+                                smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
+                            const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
+                            const uint32_t dt = tmem_base + acc * COLS + mw * N;
 #pragma unroll
-                        for (int kk = 0; kk < kHeadDim / 32; ++kk)
-                            mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
-                        mma_commit(tfull_bar0 + 8u * acc);
+                            for (int kk = 0; kk < kHeadDim / 32; ++kk)
+                                mma_f8(dt, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                            mma_commit(tfull_bar0 + 8u * acc);
+                        }
                         last_acc = acc;
                         last_ph = aph;
                         ++done;
-                    } else {
+                    } else if (lane == 0) {
                         mbar_arrive(tfull_bar0 + 8u * acc);   // nothing issued for this sub-tile
                     }
+                    __syncwarp();
                     if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
                     if (++acc == NACC) { acc = 0; aph ^= 1; }
                 }
