@@ -85,20 +85,26 @@ __host__ __device__ constexpr int tmem_cols_of(int n_pad)
                                                                 : 512;
 }
 
-struct SubDesc {
-    int b;       // request
-    int j;       // first block within the request
-    int cnt;     // blocks (1 or 2); 0 = no sub-tile here
-    int len;     // min(seq_lens[b], max_context)
-    int flags;   // kTileFirst | kTileLast | (q slot << 4)
-    int pad[3];
+// One sub-tile of a stage, 16 bytes, so that a consumer reads it with one
+// vector load: b = request, j = first block within it, len =
+// min(seq_lens[b], max_context), meta = block count (1 or 2; 0 = no sub-tile
+// here) | kTileFirst/kTileLast << 8 | q slot << 12, or kStageEnd in the first
+// sub-tile of the stage after the CTA's last.
+struct __align__(16) SubDesc {
+    int b, j, len, meta;
 };
-
 struct StageDesc {
     SubDesc sub[2];
-    int end;     // 1: no more work for this CTA
-    int pad[7];
 };
+constexpr int kMetaFirst = kTileFirst << 8;
+constexpr int kMetaLast = kTileLast << 8;
+constexpr int kMetaSlotShift = 12;
+constexpr int kStageEnd = 1 << 20;
+__device__ __forceinline__ int4 load_sub(const StageDesc* d, int i)
+{
+    return *reinterpret_cast<const int4*>(&d->sub[i]);
+}
+__device__ __forceinline__ int meta_slot(int meta) { return (meta >> kMetaSlotShift) & 1; }
 
 struct Layout {
     uint32_t k, q, s, w, desc, bar, misc, total;
@@ -460,17 +466,13 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                     // publish the stage: each owner lane its sub-tile, lane 0 the rest
                     StageDesc& sd = descs[s];
                     if (own) {
-                        SubDesc& d = sd.sub[i];
-                        d.b = win.b;
-                        d.j = win.j;
-                        d.cnt = win.cnt;
-                        d.len = win.len;
-                        d.flags = (win.first ? kTileFirst : 0) | (win.last ? kTileLast : 0) |
-                                  ((qidx & 1) << 4);
+                        const int meta = win.cnt | (win.first ? kMetaFirst : 0) |
+                                         (win.last ? kMetaLast : 0) | ((qidx & 1) << kMetaSlotShift);
+                        *reinterpret_cast<int4*>(&sd.sub[i]) = make_int4(win.b, win.j, win.len, meta);
                     }
                     if (lane == 0) {
-                        for (int k = win.n - o0; k < KT; ++k) sd.sub[k].cnt = 0;
-                        sd.end = 0;
+                        for (int k = win.n - o0; k < KT; ++k)
+                            *reinterpret_cast<int4*>(&sd.sub[k]) = make_int4(0, 0, 0, 0);
                     }
                     const unsigned m0 = __ballot_sync(0xffffffffu, own && win.ld0);
                     const unsigned m1 = __ballot_sync(0xffffffffu, own && win.ld1);
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 // end marker for the MMA and epilogue warps, in the stage after the last one
                 ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
                 if (ok) {
-                    descs[s].end = 1;
+                    *reinterpret_cast<int4*>(&descs[s].sub[0]) = make_int4(0, 0, 0, kStageEnd);
                     mbar_arrive(full_bar0 + 8u * s);
                 }
             }
@@ -534,25 +536,27 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 while (true) {
                     ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
                     if (!ok) break;
-                    const StageDesc& sd = descs[s];
-                    if (sd.end) break;
+                    const int4 x0 = load_sub(descs + s, 0);
+                    const int4 x1 = KT == 2 ? load_sub(descs + s, 1) : make_int4(0, 0, 0, 0);
+                    if (x0.w & kStageEnd) break;
                     ok = mbar_wait<kCallWait>(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
                     if (!ok) break;
                     // q / weights of every request that starts in this stage, in order
 #pragma unroll
                     for (int i = 0; i < KT; ++i) {
-                        if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
-                            ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
-                                           (qcount >> 1) & 1, abort_flag, a.status);
+                        const int meta = i == 0 ? x0.w : x1.w;
+                        if (ok && (meta & kMetaFirst)) {
+                            ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * meta_slot(meta),
+                                                      (qcount >> 1) & 1, abort_flag, a.status);
                             ++qcount;
                         }
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    const int cnt = sd.sub[mw].cnt;
-                    if (cnt != 0) {
+                    const int mmeta = mw == 0 ? x0.w : x1.w;
+                    if ((mmeta & 0xff) != 0) {
                         if (lane == 0) {
-                            const int slot = (sd.sub[mw].flags >> 4) & 1;
+                            const int slot = meta_slot(mmeta);
                             const uint64_t ad =
                                 smem_desc_sw128(k_base + s * kStageKeyBytes + mw * kSubKeyBytes);
                             const uint64_t bd = smem_desc_sw128(q_base + slot * L.q_bytes);
@@ -601,15 +605,17 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
         while (true) {
             ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
             if (!ok) break;
-            const StageDesc& sd = descs[s];
-            if (sd.end) break;
+            const int4 x0 = load_sub(descs + s, 0);
+            const int4 x1 = KT == 2 ? load_sub(descs + s, 1) : make_int4(0, 0, 0, 0);
+            if (x0.w & kStageEnd) break;
             // every warp waits for each request's q/weights in order, so that
             // its release of the slot below can never run a phase ahead
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
-                if (ok && sd.sub[i].cnt != 0 && (sd.sub[i].flags & kTileFirst)) {
-                    ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * ((sd.sub[i].flags >> 4) & 1),
-                                   (qcount >> 1) & 1, abort_flag, a.status);
+                const int meta = i == 0 ? x0.w : x1.w;
+                if (ok && (meta & kMetaFirst)) {
+                    ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * meta_slot(meta), (qcount >> 1) & 1,
+                                              abort_flag, a.status);
                     ++qcount;
                 }
             }
@@ -621,28 +627,27 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             // longer read: take the descriptor fields and this key's scales
             // into registers and hand the stage back to the producers before
             // the arithmetic, which then overlaps with the next copies.
-            SubDesc d[NSUB];
+            int4 d[NSUB];   // (request, block, length, meta) of each sub-tile taken
             float sp[NSUB];
 #pragma unroll
             for (int ii = 0; ii < NSUB; ++ii) {
                 const int i = E::kSubSplit ? grp : ii;
-                d[ii] = sd.sub[i];
+                d[ii] = E::kSubSplit ? (grp == 0 ? x0 : x1) : (ii == 0 ? x0 : x1);
                 sp[ii] = scales_smem[s * (kStageScaleBytes / 4) + i * kTileKeys + row];
             }
-            int rel0 = -1, rel1 = -1;
-            if (sd.sub[0].cnt != 0 && (sd.sub[0].flags & kTileLast)) rel0 = (sd.sub[0].flags >> 4) & 1;
-            if (KT == 2 && sd.sub[1].cnt != 0 && (sd.sub[1].flags & kTileLast))
-                rel1 = (sd.sub[1].flags >> 4) & 1;
+            const int rel0 = (x0.w & kMetaLast) ? meta_slot(x0.w) : -1;
+            const int rel1 = (KT == 2 && (x1.w & kMetaLast)) ? meta_slot(x1.w) : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar0 + 8u * s);
 #pragma unroll
             for (int ii = 0; ii < NSUB; ++ii) {
                 const int i = E::kSubSplit ? grp : ii;
-                if (d[ii].cnt == 0) continue;
-                if (d[ii].b != cur_b) {
+                const int dcnt = d[ii].w & 0xff;
+                if (dcnt == 0) continue;
+                if (d[ii].x != cur_b) {
                     // first sub-tile of a new request for this warp
                     const float4* w4 = reinterpret_cast<const float4*>(
-                        smem + L.w + ((d[ii].flags >> 4) & 1) * L.w_bytes);
+                        smem + L.w + meta_slot(d[ii].w) * L.w_bytes);
 #pragma unroll
                     for (int k = 0; k < E::SL; ++k) {
                         const int t = first_slot + k * E::GS;
@@ -654,11 +659,11 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                             wp[(k * H + h) / 2 + 1] = pack2(v.z, v.w);
                         }
                     }
-                    cur_b = d[ii].b;
+                    cur_b = d[ii].x;
                 }
-                const int pos = (d[ii].j + page) * kBlockKeys + key;
-                const bool valid = page < d[ii].cnt && pos < d[ii].len;
-                float* orow = a.out + (long long)d[ii].b * NN * a.out_stride + pos;
+                const int pos = (d[ii].y + page) * kBlockKeys + key;
+                const bool valid = page < dcnt && pos < d[ii].z;
+                float* orow = a.out + (long long)d[ii].x * NN * a.out_stride + pos;
                 const uint32_t taddr = lane_addr + acc * COLS + i * N;
                 if constexpr (NN % E::GS != 0) {
                     if (short_group) {
