@@ -144,38 +144,61 @@ __device__ __forceinline__ void tmem_wait_bind(uint32_t (&r)[W])
     else tmem_wait_bind8(r);
 }
 
-// The logits of this thread's key for SL slots t = first_slot + k*GS
-// (k < SL): the head scores are read from TMEM in chunks of up to CWMAX
-// columns, the load of the next chunk issued before the current one is
-// rectified, weighted (packed f32x2 FMAs, eight lanes of accumulators) and
-// summed, so TMEM latency hides behind the arithmetic.  taddr0 is the column
-// of slot 0 in this thread's lane; wp holds the weights of the SL slots as
-// packed pairs (heads 2i, 2i+1 of slot k at wp[k*H/2 + i]).
-template <int H, int SL, int GS, int CWMAX, int WN>
-__device__ __forceinline__ void slot_logits(uint32_t taddr0, const uint64_t (&wp)[WN],
-                                            int first_slot, float sp, bool valid,
-                                            float* __restrict__ orow, long long out_stride)
+// The logits of this thread's key for every (sub-tile, slot) pass of a stage:
+// NS sub-tiles x SL slots t = first_slot + k*GS.  The head scores are read
+// from TMEM in chunks of up to CWMAX columns as one pipelined sequence, the
+// load of the next chunk issued before the current one is computed (across
+// pass boundaries too, so only the stage's first load is waited for in
+// full), then rectified, weighted (packed f32x2 FMAs, four accumulators) and
+// summed.  taddr[n] is the column of slot 0 of sub-tile n in this thread's
+// lane.  wp holds packed weight pairs of the SL slots (slot k at
+// wp[k*H/2 + i]) of request cur_b; a sub-tile of another request reloads them
+// from its shared-memory weights wsrc[n] before its first chunk.  A sub-tile
+// with no blocks (d.w == 0) is computed on stale columns and not stored.
+template <int H, int NN, int NS, int SL, int GS, int CWMAX, int WN>
+__device__ __forceinline__ void stage_logits(const uint32_t (&taddr)[NS], const int4 (&d)[NS],
+                                             const float (&sp)[NS], const bool (&valid)[NS],
+                                             float* const (&orow)[NS],
+                                             const float4* const (&wsrc)[NS], uint64_t (&wp)[WN],
+                                             int& cur_b, int first_slot, long long out_stride)
 {
     static_assert(SL * H / 2 <= WN, "weights of every slot are held");
     constexpr int CW = H >= CWMAX ? CWMAX : H;   // chunk width (columns)
     constexpr int CPS = H / CW;                  // chunks per slot
-    constexpr int NC = SL * CPS;
+    constexpr int CPP = SL * CPS;                // chunks per sub-tile
+    constexpr int NC = NS * CPP;
+    auto column = [&](int c) {
+        return taddr[c / CPP] + (uint32_t)((first_slot + ((c % CPP) / CPS) * GS) * H + (c % CPS) * CW);
+    };
     uint32_t buf[2][CW];
     uint64_t acc[4];
-    tmem_ld_async<CW>(taddr0 + first_slot * H, buf[0]);
+    tmem_ld_async<CW>(column(0), buf[0]);
     tmem_wait_bind<CW>(buf[0]);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        const int k = c / CPS;
+        const int n = c / CPP;
+        const int k = (c % CPP) / CPS;
         const int t = first_slot + k * GS;
+        if (c % CPP == 0 && (d[n].w & 0xff) != 0 && d[n].x != cur_b) {
+            // first sub-tile of a new request for this warp
+#pragma unroll
+            for (int kk = 0; kk < SL; ++kk) {
+                const int tt = first_slot + kk * GS;
+#pragma unroll
+                for (int h = 0; h < H; h += 4) {
+                    const float4 v = tt < NN ? wsrc[n][tt * (H / 4) + h / 4]
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    wp[(kk * H + h) / 2] = pack2(v.x, v.y);
+                    wp[(kk * H + h) / 2 + 1] = pack2(v.z, v.w);
+                }
+            }
+            cur_b = d[n].x;
+        }
         if (c % CPS == 0) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) acc[a] = 0ull;
         }
-        if (c + 1 < NC) {
-            const int tn = first_slot + ((c + 1) / CPS) * GS;
-            tmem_ld_async<CW>(taddr0 + tn * H + ((c + 1) % CPS) * CW, buf[(c + 1) & 1]);
-        }
+        if (c + 1 < NC) tmem_ld_async<CW>(column(c + 1), buf[(c + 1) & 1]);
         const uint32_t(&v)[CW] = buf[c & 1];
         const int w0 = (k * H + (c % CPS) * CW) / 2;
 #pragma unroll
@@ -186,7 +209,7 @@ __device__ __forceinline__ void slot_logits(uint32_t taddr0, const uint64_t (&wp
         }
         if (c % CPS == CPS - 1) {
             const float r = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
-            if (valid) orow[(long long)t * out_stride] = sp * r;
+            if (valid[n] && t < NN) orow[n][(long long)t * out_stride] = sp[n] * r;
         }
         if (c + 1 < NC) tmem_wait_bind<CW>(buf[(c + 1) & 1]);
     }
@@ -595,7 +618,6 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
         // sub-tiles of each stage this group processes, and its slots
         constexpr int NSUB = E::kSubSplit ? 1 : KT;
         const int first_slot = E::kSubSplit ? 0 : grp;
-        const bool short_group = first_slot + (E::SL - 1) * E::GS >= NN;   // one slot fewer
         uint64_t wp[E::kWeightPairs];
         int cur_b = -1;                        // request whose weights wp holds
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
@@ -639,41 +661,37 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             const int rel1 = (KT == 2 && (x1.w & kMetaLast)) ? meta_slot(x1.w) : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar0 + 8u * s);
+            uint32_t taddr[NSUB];
+            bool valid[NSUB];
+            float* orow[NSUB];
+            const float4* wsrc[NSUB];
 #pragma unroll
             for (int ii = 0; ii < NSUB; ++ii) {
                 const int i = E::kSubSplit ? grp : ii;
-                const int dcnt = d[ii].w & 0xff;
-                if (dcnt == 0) continue;
-                if (d[ii].x != cur_b) {
-                    // first sub-tile of a new request for this warp
-                    const float4* w4 = reinterpret_cast<const float4*>(
-                        smem + L.w + meta_slot(d[ii].w) * L.w_bytes);
-#pragma unroll
-                    for (int k = 0; k < E::SL; ++k) {
-                        const int t = first_slot + k * E::GS;
-#pragma unroll
-                        for (int h = 0; h < H; h += 4) {
-                            const float4 v = t < NN ? w4[t * (H / 4) + h / 4]
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                            wp[(k * H + h) / 2] = pack2(v.x, v.y);
-                            wp[(k * H + h) / 2 + 1] = pack2(v.z, v.w);
-                        }
-                    }
-                    cur_b = d[ii].x;
-                }
                 const int pos = (d[ii].y + page) * kBlockKeys + key;
-                const bool valid = page < dcnt && pos < d[ii].z;
-                float* orow = a.out + (long long)d[ii].x * NN * a.out_stride + pos;
-                const uint32_t taddr = lane_addr + acc * COLS + i * N;
-                if constexpr (NN % E::GS != 0) {
-                    if (short_group) {
-                        slot_logits<H, E::SL - 1, E::GS, E::kChunk>(
-                            taddr, wp, first_slot, sp[ii], valid, orow, a.out_stride);
-                        continue;
-                    }
+                taddr[ii] = lane_addr + acc * COLS + i * N;
+                valid[ii] = page < (d[ii].w & 0xff) && pos < d[ii].z;
+                orow[ii] = a.out + (long long)d[ii].x * NN * a.out_stride + pos;
+                wsrc[ii] = reinterpret_cast<const float4*>(smem + L.w + meta_slot(d[ii].w) * L.w_bytes);
+            }
+            if constexpr (NSUB == 1) {
+                stage_logits<H, NN, 1, E::SL, E::GS, E::kChunk>(taddr, d, sp, valid, orow, wsrc, wp,
+                                                                 cur_b, first_slot, a.out_stride);
+            } else {
+                // two sub-tiles: one pipelined pass each (measured faster than
+                // one sequence over both at these register counts)
+#pragma unroll
+                for (int ii = 0; ii < NSUB; ++ii) {
+                    if ((d[ii].w & 0xff) == 0) continue;
+                    const uint32_t ta1[1] = {taddr[ii]};
+                    const int4 d1[1] = {d[ii]};
+                    const float sp1[1] = {sp[ii]};
+                    const bool v1[1] = {valid[ii]};
+                    float* const o1[1] = {orow[ii]};
+                    const float4* const w1[1] = {wsrc[ii]};
+                    stage_logits<H, NN, 1, E::SL, E::GS, E::kChunk>(ta1, d1, sp1, v1, o1, w1, wp,
+                                                                     cur_b, first_slot, a.out_stride);
                 }
-                slot_logits<H, E::SL, E::GS, E::kChunk>(taddr, wp, first_slot, sp[ii], valid,
-                                                        orow, a.out_stride);
             }
             tc_fence_before();
             __syncwarp();
