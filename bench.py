@@ -280,6 +280,8 @@ def main():
                     help="rotate: cycle through --copies resident input sets (together larger "
                          "than L2) with back-to-back launches; flush: write 256 MiB between steps")
     ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--out-dtype", default="float32", choices=["float32", "bfloat16"],
+                    help="fp8 workloads: element type of the logits (the output_dtype option)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -313,17 +315,18 @@ def main():
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     copies = args.copies if args.l2 == "rotate" else 1
+    out_dtype = torch.bfloat16 if (is_fp8 and args.out_dtype == "bfloat16") else torch.float32
     if is_fp8:
         def device_set():
             return dict(q=t(p.q), kv=t(p.kv_fused), w=t(p.weights), sl=t(p.seq_lens),
                         bt=t(p.block_table),
-                        out=torch.zeros((p.batch * p.next_n, p.max_context), dtype=torch.float32,
+                        out=torch.zeros((p.batch * p.next_n, p.max_context), dtype=out_dtype,
                                         device=dev))
         sets = [device_set() for _ in range(copies)]
 
         def step(d, stream=None):
-            pml.pml_fp8_paged_mqa_logits(d["q"], d["kv"], d["w"], d["sl"], d["bt"], d["out"],
-                                         p.max_context, p.next_n, stream=stream)
+            pml.pml_fp8_paged_mqa_logits_ex(d["q"], d["kv"], d["w"], d["sl"], d["bt"], d["out"],
+                                            p.max_context, p.next_n, stream=stream)
         kernel = "fp8_logits_kernel"
         bound_name = "hbm"
     else:
@@ -390,7 +393,7 @@ def main():
         hq, hkv, hw = (torch.from_numpy(a).pin_memory() for a in (p.q, p.kv_fused, p.weights))
         hsl, hbt = torch.from_numpy(p.seq_lens).pin_memory(), torch.from_numpy(p.block_table).pin_memory()
         d0 = sets[0]
-        hout = torch.empty(d0["out"].shape, dtype=torch.float32).pin_memory()
+        hout = torch.empty(d0["out"].shape, dtype=out_dtype).pin_memory()
         inputs = ((d0["q"], hq), (d0["kv"], hkv), (d0["w"], hw), (d0["sl"], hsl), (d0["bt"], hbt))
         h2d = sum(h.numel() * h.element_size() for _, h in inputs)
         d2h = hout.numel() * hout.element_size()
@@ -432,7 +435,7 @@ def main():
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    alg_bytes = p.algorithmic_bytes()
+    alg_bytes = p.algorithmic_bytes(out_dtype.itemsize) if is_fp8 else p.algorithmic_bytes()
     achieved_gbs = alg_bytes / avg_launch_s / 1e9
     roof = {"bound": bound_name, "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved_gbs / hbm_peak, "traffic": recorded_traffic(kernel, args.workload),
@@ -446,9 +449,11 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 x e4m3 -> f32" if is_fp8 else "bf16 x bf16 -> f32",
+            "dtype": (("e4m3 x e4m3 -> f32" + (" -> bf16 out" if out_dtype == torch.bfloat16 else ""))
+                      if is_fp8 else "bf16 x bf16 -> f32"),
             "data": "synthetic (seeded generators; no public dataset on the pages)",
-            "config": config_of(args.workload, p, world, args.l2, copies),
+            "config": dict(config_of(args.workload, p, world, args.l2, copies),
+                           **({"output_dtype": args.out_dtype} if is_fp8 else {})),
             "clocks": clocks.summary(), "gpu_launches": args.steps,
             "e2e": e2e, "roofline": roof,
             "logits_per_s": positions_all * getattr(p, "next_n", 1) * args.steps / total_s,

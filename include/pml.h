@@ -125,6 +125,33 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
                              int64_t out_stride, int max_context, int batch, int next_n,
                              int num_heads, void* stream);
 
+/* Output element types of pml_fp8_paged_mqa_logits_ex. */
+#define PML_DTYPE_FLOAT32 0
+#define PML_DTYPE_BFLOAT16 1
+
+/*
+ * pml_fp8_paged_mqa_logits_ex -- pml_fp8_paged_mqa_logits with the pages'
+ * output_dtype option ("flashinfer.attn_scores": the paragraph comparing the
+ * two variants -- the fp8 call exposes acc_dtype and output_dtype, output
+ * float32 by default).
+ *
+ * output_dtype  PML_DTYPE_FLOAT32: `out` is fp32, exactly as
+ *               pml_fp8_paged_mqa_logits (which is this call with that value);
+ *               PML_DTYPE_BFLOAT16: `out` is bf16 [batch*next_n, out_stride]
+ *               (2-byte aligned), each logit the fp32 result rounded to
+ *               nearest even.  The accumulator is fp32 in both cases (the
+ *               tensor cores' f32 accumulation; no other acc_dtype is
+ *               offered).  Other values return PML_ERR_UNSUPPORTED.
+ * All other arguments, the written region and the errors are those of
+ * pml_fp8_paged_mqa_logits; out_stride counts elements of the output type.
+ */
+int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
+                                const float* weights, const int32_t* seq_lens,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* schedule_meta, int num_ctas, void* out,
+                                int64_t out_stride, int output_dtype, int max_context, int batch,
+                                int next_n, int num_heads, void* stream);
+
 /*
  * pml_indexer_scores_bf16 ("flashinfer.sdsa.indexer_scores": body and the
  * query, key_cache, block_table, context_lengths, requests and scores

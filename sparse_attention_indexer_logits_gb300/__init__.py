@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
   ("flashinfer.attn_scores", "Scheduling and Setup").
 * ``pml_fp8_paged_mqa_logits`` -- ``out[b*n+t, p] = s_p * sum_h w * relu(q.k_p)``
   over an fp8 paged ``kv_fused`` cache ("flashinfer.attn_scores").
+* ``pml_fp8_paged_mqa_logits_ex`` -- the same with the ``output_dtype``
+  option (fp32 or bf16 logits).
 * ``pml_indexer_scores_bf16`` -- the single-head bf16 case
   ("flashinfer.sdsa.indexer_scores").
 
@@ -27,6 +29,7 @@ import torch
 
 __all__ = [
     "PmlError", "lib", "library_path", "pml_schedule", "pml_fp8_paged_mqa_logits",
+    "pml_fp8_paged_mqa_logits_ex",
     "pml_indexer_scores_bf16", "pml_fp8_paged_mqa_logits_noalloc", "pml_device_status",
     "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
     "fp8_paged_mqa_logits", "indexer_scores", "compute_paged_mqa_logits_schedule",
@@ -75,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.pml_fp8_paged_mqa_logits.argtypes = [P, P, i64, P, P, P, i64, P, i32, P, i64, i32, i32,
                                                i32, i32, P]
         L.pml_fp8_paged_mqa_logits.restype = i32
+        L.pml_fp8_paged_mqa_logits_ex.argtypes = [P, P, i64, P, P, P, i64, P, i32, P, i64, i32, i32,
+                                                  i32, i32, i32, P]
+        L.pml_fp8_paged_mqa_logits_ex.restype = i32
         L.pml_indexer_scores_bf16.argtypes = [P, i32, P, i64, i64, P, i64, i32, P, P, i32, P, i64,
                                               i32, P]
         L.pml_indexer_scores_bf16.restype = i32
@@ -189,6 +195,46 @@ def pml_fp8_paged_mqa_logits(q: torch.Tensor, kv_fused: torch.Tensor, weights: t
     return out
 
 
+_OUT_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def pml_fp8_paged_mqa_logits_ex(q: torch.Tensor, kv_fused: torch.Tensor, weights: torch.Tensor,
+                                seq_lens: torch.Tensor, block_table: torch.Tensor,
+                                out: torch.Tensor, max_context: int, next_n: int,
+                                schedule_meta: torch.Tensor | None = None, num_ctas: int = 0,
+                                stream=None) -> torch.Tensor:
+    """``pml_fp8_paged_mqa_logits`` writing ``out`` in its own dtype: fp32, or
+    bf16 (the fp32 logit rounded to nearest even)."""
+    if out.dtype not in _OUT_DTYPES:
+        raise ValueError("out must be float32 or bfloat16")
+    for t, nm in ((q, "q"), (kv_fused, "kv_fused"), (weights, "weights"), (seq_lens, "seq_lens")):
+        _cuda(t, nm)
+    _cuda(block_table, "block_table", contiguous=False)
+    _cuda(out, "out", contiguous=False)
+    if block_table.stride(-1) != 1 or out.stride(-1) != 1:
+        raise ValueError("block_table and out need unit stride in their last dimension")
+    if q.dim() != 3 or q.shape[2] != 128 or q.element_size() != 1:
+        raise ValueError("q must be [batch*next_n, heads, 128] with 1-byte elements")
+    if weights.dtype != torch.float32:
+        raise ValueError("weights must be float32")
+    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise ValueError("seq_lens and block_table must be int32")
+    batch = seq_lens.numel()
+    H = q.shape[1]
+    if q.shape[0] != batch * next_n or tuple(weights.shape) != (batch * next_n, H):
+        raise ValueError("q / weights rows must be batch*next_n")
+    if kv_fused.numel() % 8448 != 0:
+        raise ValueError("kv_fused must hold whole 8448-byte blocks")
+    if out.shape[0] < batch * next_n or out.shape[1] < max_context:
+        raise ValueError("out too small")
+    _check(lib().pml_fp8_paged_mqa_logits_ex(
+        _ptr(q), _ptr(kv_fused), kv_fused.numel() // 8448, _ptr(weights), _ptr(seq_lens),
+        _ptr(block_table), block_table.stride(0), _ptr(schedule_meta), num_ctas, _ptr(out),
+        out.stride(0), _OUT_DTYPES[out.dtype], max_context, batch, next_n, H, _stream(stream)),
+        "pml_fp8_paged_mqa_logits_ex")
+    return out
+
+
 def pml_indexer_scores_bf16(query: torch.Tensor, key_cache: torch.Tensor, page_stride_bytes: int,
                             num_pages: int, block_table: torch.Tensor,
                             context_lengths: torch.Tensor, requests: torch.Tensor,
@@ -248,21 +294,25 @@ def compute_paged_mqa_logits_schedule(seq_lens: torch.Tensor, next_n: int = 1,
 
 
 def fp8_paged_mqa_logits(q, kv_fused, weights, seq_lens, block_table, *, max_context=None,
-                         schedule_meta=None, out=None, num_ctas=None):
-    """Keyword-style wrapper.  ``out`` is allocated (filled with -inf) only
-    when not given; rows of empty requests and positions past each request's
-    length are never written."""
+                         schedule_meta=None, out=None, num_ctas=None, output_dtype=None):
+    """Keyword-style wrapper.  ``out`` is allocated (filled with -inf, of
+    ``output_dtype``: float32 by default, or bfloat16) only when not given;
+    rows of empty requests and positions past each request's length are never
+    written."""
     batch = seq_lens.numel()
     next_n = q.shape[0] // max(batch, 1)
     if max_context is None:
         max_context = block_table.shape[1] * 64
     if out is None:
-        out = torch.full((q.shape[0], max_context), float("-inf"), dtype=torch.float32,
-                         device=q.device)
+        out = torch.full((q.shape[0], max_context), float("-inf"),
+                         dtype=output_dtype or torch.float32, device=q.device)
+    elif output_dtype is not None and out.dtype != output_dtype:
+        raise ValueError("out and output_dtype disagree")
     if num_ctas is None:
         num_ctas = (schedule_meta.numel() // 2 - 1) if schedule_meta is not None else 0
-    return pml_fp8_paged_mqa_logits(q, kv_fused, weights, seq_lens, block_table, out, max_context,
-                                    next_n, schedule_meta=schedule_meta, num_ctas=num_ctas)
+    return pml_fp8_paged_mqa_logits_ex(q, kv_fused, weights, seq_lens, block_table, out,
+                                       max_context, next_n, schedule_meta=schedule_meta,
+                                       num_ctas=num_ctas)
 
 
 def indexer_scores(query, key_cache, block_table, context_lengths, *, requests, scores,

@@ -105,7 +105,7 @@ cudaError_t encode_sw128(CUtensorMap& map, CUtensorMapDataType dtype, int rank, 
 
 extern "C" {
 
-int pml_version(void) { return 100; }
+int pml_version(void) { return 101; }
 
 const char* pml_error_string(int code)
 {
@@ -159,7 +159,23 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
                              int64_t out_stride, int max_context, int batch, int next_n,
                              int num_heads, void* stream)
 {
+    return pml_fp8_paged_mqa_logits_ex(q, kv_fused, num_blocks, weights, seq_lens, block_table,
+                                       bt_stride, schedule_meta, num_ctas, out, out_stride,
+                                       PML_DTYPE_FLOAT32, max_context, batch, next_n, num_heads,
+                                       stream);
+}
+
+int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
+                                const float* weights, const int32_t* seq_lens,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* schedule_meta, int num_ctas, void* out,
+                                int64_t out_stride, int output_dtype, int max_context, int batch,
+                                int next_n, int num_heads, void* stream)
+{
     if (batch < 0 || num_ctas < 0) return PML_ERR_INVALID_ARG;
+    if (output_dtype != PML_DTYPE_FLOAT32 && output_dtype != PML_DTYPE_BFLOAT16)
+        return PML_ERR_UNSUPPORTED;
+    const int out_bytes = output_dtype == PML_DTYPE_BFLOAT16 ? 2 : 4;
     if (next_n < 1 || next_n > 4) return PML_ERR_UNSUPPORTED;
     if (num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64)
         return PML_ERR_UNSUPPORTED;
@@ -171,7 +187,7 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
     const long long rows_total = (long long)batch * next_n * num_heads;
     if (rows_total > 0x7fffffffLL) return PML_ERR_INVALID_ARG;
     if (schedule_meta != nullptr && num_ctas == 0) return PML_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16) || !aligned(out, 4) ||
+    if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16) || !aligned(out, out_bytes) ||
         !aligned(seq_lens, 4) || !aligned(block_table, 4) || !aligned(schedule_meta, 4))
         return PML_ERR_ALIGNMENT;
 
@@ -187,6 +203,7 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
     a.weights = weights;
     a.kv_fused = kv_fused;
     a.out = out;
+    a.out_bf16 = output_dtype == PML_DTYPE_BFLOAT16 ? 1 : 0;
     a.status = dev.status;
     a.bt_stride = bt_stride;
     a.out_stride = out_stride;
@@ -200,7 +217,6 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
     const size_t per_stage = fp8_smem_bytes(next_n, num_heads, 1) - fixed;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
     if (stages > kMaxFp8Stages) stages = kMaxFp8Stages;
-    stages &= ~1;                        // two producers take even / odd stages
     if (stages < 2) return PML_ERR_UNSUPPORTED;
     a.stages = stages;
 

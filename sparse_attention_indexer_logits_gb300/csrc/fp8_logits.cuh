@@ -43,6 +43,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -151,16 +152,24 @@ __device__ __forceinline__ void tmem_wait_bind(uint32_t (&r)[W])
 // pass boundaries too, so only the stage's first load is waited for in
 // full), then rectified, weighted (packed f32x2 FMAs, four accumulators) and
 // summed.  taddr[n] is the column of slot 0 of sub-tile n in this thread's
-// lane.  wp holds packed weight pairs of the SL slots (slot k at
+// lane and oidx[n] the output element of its slot 0.  wp holds packed weight pairs of the SL slots (slot k at
 // wp[k*H/2 + i]) of request cur_b; a sub-tile of another request reloads them
 // from its shared-memory weights wsrc[n] before its first chunk.  A sub-tile
 // with no blocks (d.w == 0) is computed on stale columns and not stored.
+// Logit v of output element idx: fp32, or bf16 rounded to nearest even.
+__device__ __forceinline__ void store_logit(void* out, bool bf16, long long idx, float v)
+{
+    if (bf16) reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    else reinterpret_cast<float*>(out)[idx] = v;
+}
+
 template <int H, int NN, int NS, int SL, int GS, int CWMAX, int WN>
 __device__ __forceinline__ void stage_logits(const uint32_t (&taddr)[NS], const int4 (&d)[NS],
                                              const float (&sp)[NS], const bool (&valid)[NS],
-                                             float* const (&orow)[NS],
+                                             const long long (&oidx)[NS],
                                              const float4* const (&wsrc)[NS], uint64_t (&wp)[WN],
-                                             int& cur_b, int first_slot, long long out_stride)
+                                             int& cur_b, int first_slot, void* out, bool out_bf16,
+                                             long long out_stride)
 {
     static_assert(SL * H / 2 <= WN, "weights of every slot are held");
     constexpr int CW = H >= CWMAX ? CWMAX : H;   // chunk width (columns)
@@ -209,7 +218,8 @@ __device__ __forceinline__ void stage_logits(const uint32_t (&taddr)[NS], const 
         }
         if (c % CPS == CPS - 1) {
             const float r = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
-            if (valid[n] && t < NN) orow[n][(long long)t * out_stride] = sp[n] * r;
+            if (valid[n] && t < NN)
+                store_logit(out, out_bf16, oidx[n] + t * out_stride, sp[n] * r);
         }
         if (c + 1 < NC) tmem_wait_bind<CW>(buf[(c + 1) & 1]);
     }
@@ -663,7 +673,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
             if (lane == 0) mbar_arrive(empty_bar0 + 8u * s);
             uint32_t taddr[NSUB];
             bool valid[NSUB];
-            float* orow[NSUB];
+            long long oidx[NSUB];
             const float4* wsrc[NSUB];
 #pragma unroll
             for (int ii = 0; ii < NSUB; ++ii) {
@@ -671,12 +681,13 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 const int pos = (d[ii].y + page) * kBlockKeys + key;
                 taddr[ii] = lane_addr + acc * COLS + i * N;
                 valid[ii] = page < (d[ii].w & 0xff) && pos < d[ii].z;
-                orow[ii] = a.out + (long long)d[ii].x * NN * a.out_stride + pos;
+                oidx[ii] = (long long)d[ii].x * NN * a.out_stride + pos;
                 wsrc[ii] = reinterpret_cast<const float4*>(smem + L.w + meta_slot(d[ii].w) * L.w_bytes);
             }
             if constexpr (NSUB == 1) {
-                stage_logits<H, NN, 1, E::SL, E::GS, E::kChunk>(taddr, d, sp, valid, orow, wsrc, wp,
-                                                                 cur_b, first_slot, a.out_stride);
+                stage_logits<H, NN, 1, E::SL, E::GS, E::kChunk>(taddr, d, sp, valid, oidx, wsrc, wp,
+                                                                 cur_b, first_slot, a.out,
+                                                                 a.out_bf16 != 0, a.out_stride);
             } else {
                 // two sub-tiles: one pipelined pass each (measured faster than
                 // one sequence over both at these register counts)
@@ -687,10 +698,11 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                     const int4 d1[1] = {d[ii]};
                     const float sp1[1] = {sp[ii]};
                     const bool v1[1] = {valid[ii]};
-                    float* const o1[1] = {orow[ii]};
+                    const long long o1[1] = {oidx[ii]};
                     const float4* const w1[1] = {wsrc[ii]};
                     stage_logits<H, NN, 1, E::SL, E::GS, E::kChunk>(ta1, d1, sp1, v1, o1, w1, wp,
-                                                                     cur_b, first_slot, a.out_stride);
+                                                                     cur_b, first_slot, a.out,
+                                                                     a.out_bf16 != 0, a.out_stride);
                 }
             }
             tc_fence_before();

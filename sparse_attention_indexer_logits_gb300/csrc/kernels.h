@@ -14,16 +14,17 @@ struct Fp8Args {
     const int32_t* schedule_meta;  // nullptr: computed by each CTA
     const float* weights;
     const uint8_t* kv_fused;
-    float* out;
+    void* out;        // fp32, or bf16 when out_bf16
     unsigned int* status;
     long long bt_stride;
-    long long out_stride;
+    long long out_stride;   // elements
     long long num_blocks;
     int batch;
     int next_n;
     int max_context;
     int stages;       // depth of the K-page ring
     int q_box_rows;   // rows one Q load brings (<= MMA N)
+    int out_bf16;     // 1: logits stored as bf16 (round to nearest even)
 };
 
 struct Bf16Args {

@@ -61,6 +61,14 @@ def sentinel_f32(shape) -> np.ndarray:
     return np.full(shape, SENTINEL_BITS, dtype=np.uint32).view(np.float32)
 
 
+SENTINEL_BF16_BITS = 0x7FDE                    # a bf16 NaN payload for bf16 outputs
+
+
+def sentinel_bf16_bits(shape) -> np.ndarray:
+    """uint16 bit patterns of a bf16 array pre-filled with the sentinel."""
+    return np.full(shape, SENTINEL_BF16_BITS, dtype=np.uint16)
+
+
 @dataclass
 class Fp8Problem:
     name: str
@@ -87,10 +95,11 @@ class Fp8Problem:
     def positions(self) -> int:
         return int(np.maximum(self.seq_lens, 0).sum())
 
-    def algorithmic_bytes(self) -> int:
+    def algorithmic_bytes(self, out_bytes: int = 4) -> int:
         """Bytes the method must move once: every valid key (128 e4m3 + one fp32
         scale), one block-table entry per block, each request's q rows and
-        weights and its length, and the fp32 logits it writes."""
+        weights and its length, and the logits it writes (out_bytes each: 4
+        for fp32, 2 for bf16)."""
         n, H = self.next_n, self.num_heads
         total = 0
         for L in self.seq_lens.tolist():
@@ -98,7 +107,7 @@ class Fp8Problem:
                 total += 4
                 continue
             total += L * (HEAD_DIM + 4) + blocks_for(L) * 4 + n * H * (HEAD_DIM + 4) + 4
-            total += n * L * 4
+            total += n * L * out_bytes
         return total
 
     def algorithmic_flops(self) -> int:

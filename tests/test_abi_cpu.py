@@ -78,6 +78,25 @@ def test_fp8_argument_checks(L):
     assert _fp8(L, out=P + 2) == 3
 
 
+def _fp8_ex(L, dtype, **over):
+    args = dict(q=P, kv=P, nb=10, w=P, sl=P, bt=P, bt_stride=4, meta=None, num_ctas=0, out=P,
+                out_stride=256, mc=256, batch=2, n=1, H=64)
+    args.update(over)
+    return L.pml_fp8_paged_mqa_logits_ex(
+        args["q"], args["kv"], args["nb"], args["w"], args["sl"], args["bt"], args["bt_stride"],
+        args["meta"], args["num_ctas"], args["out"], args["out_stride"], dtype, args["mc"],
+        args["batch"], args["n"], args["H"], None)
+
+
+def test_fp8_output_dtype_checks(L):
+    assert _fp8_ex(L, 2) == 2 and _fp8_ex(L, -1) == 2  # only fp32 (0) and bf16 (1)
+    assert _fp8_ex(L, 1, batch=0) == 0
+    assert _fp8_ex(L, 1, out=P + 2, n=0) == 2          # shape checks still come first
+    assert _fp8_ex(L, 1, out=P + 1) == 3               # bf16 out: 2-byte alignment
+    assert _fp8_ex(L, 0, out=P + 2) == 3               # fp32 out: 4-byte alignment
+    assert _fp8_ex(L, 1, out_stride=100) == 1
+
+
 def _bf16(L, **over):
     a = dict(q=P, rows=8, kc=P, stride=16384, pages=4, bt=P, bt_stride=4, nreq=2, cl=P, req=P,
              groups=2, sc=P, sc_stride=256, mc=256)
