@@ -70,6 +70,13 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_int,
     ]
     lib.orc_indexer_scores_bf16.restype = ctypes.c_int
+    lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_decode.restype = ctypes.c_double
+    lib.orc_indexer_scores_nvfp4.argtypes = [
+        P, P, ctypes.c_int, P, i64, P, i64, P, i64, P, P, ctypes.c_int, P, P, i64,
+        ctypes.c_int, ctypes.c_int,
+    ]
+    lib.orc_indexer_scores_nvfp4.restype = ctypes.c_int
     return lib
 
 
@@ -108,6 +115,11 @@ def default_threads() -> int:
 def e4m3_decode(code: int) -> float:
     """Value of an E4M3FN byte (OCP 8-bit float: bias 7, 0x7F/0xFF NaN)."""
     return _load().orc_e4m3_decode(int(code) & 0xFF)
+
+
+def e2m1_decode(code: int) -> float:
+    """Value of a 4-bit E2M1 code (OCP FP4: bias 1, one mantissa bit)."""
+    return _load().orc_e2m1_decode(int(code) & 0xF)
 
 
 def bf16_decode(bits: int) -> float:
@@ -198,6 +210,49 @@ def indexer_scores_bf16(query, key_cache, page_stride_bytes: int, block_table, c
         _ptr(qy), rows, _ptr(kc), int(page_stride_bytes), _ptr(bt), bt.shape[1], _ptr(cl),
         _ptr(rq), cl.shape[0], _ptr(out), _ptr(mag) if mag is not None else None,
         out.shape[1], max_context, nthreads or default_threads(),
+    )
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out, mag
+
+
+def indexer_scores_nvfp4(query, query_scales, key_cache, page_stride_bytes: int, key_scales,
+                         scale_page_stride_bytes: int, block_table, context_lengths, requests,
+                         max_context: int, out=None, with_mag: bool = True,
+                         nthreads: int | None = None):
+    """fp64 single-head scores over NVFP4 queries and keys
+    ("flashinfer.sdsa.indexer_scores": the NVFP4 forms of ``query``,
+    ``key_cache``, ``query_scales`` and ``key_scales``).  Element ``d`` of a
+    row is the E2M1 code in byte ``d//2`` (low nibble for even ``d``) times the
+    row's E4M3 scale ``d//16``; a score is the plain dot product of the
+    dequantised query row and key.  Groups are uniform as in
+    ``indexer_scores_bf16``.
+
+    ``query`` uint8 ``[rows, 64]``, ``query_scales`` uint8 ``[rows, 8]``;
+    ``key_cache`` / ``key_scales`` raw bytes, page ``P`` at byte
+    ``P*page_stride_bytes`` (64x64 packed bytes) and
+    ``P*scale_page_stride_bytes`` (64x8 scale bytes).  Returns
+    ``(scores, mag)``, ``mag`` = ``sum_d |q_d k_d|``; entries past a group's
+    length are left as they were.
+    """
+    qy = _c(query, np.uint8)
+    qs = _c(query_scales, np.uint8)
+    kc = _c(np.asarray(key_cache).view(np.uint8), np.uint8).reshape(-1)
+    ks = _c(np.asarray(key_scales).view(np.uint8), np.uint8).reshape(-1)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lengths, np.int32)
+    rq = _c(requests, np.int32)
+    rows = qy.shape[0]
+    assert qy.shape[1] == 64 and qs.shape == (rows, 8)
+    if out is None:
+        out = np.full((rows, max_context), np.nan, dtype=np.float64)
+    assert out.dtype == np.float64 and out.flags.c_contiguous
+    mag = np.full(out.shape, np.nan, dtype=np.float64) if with_mag else None
+    rc = _load().orc_indexer_scores_nvfp4(
+        _ptr(qy), _ptr(qs), rows, _ptr(kc), int(page_stride_bytes), _ptr(ks),
+        int(scale_page_stride_bytes), _ptr(bt), bt.shape[1], _ptr(cl), _ptr(rq), cl.shape[0],
+        _ptr(out), _ptr(mag) if mag is not None else None, out.shape[1], max_context,
+        nthreads or default_threads(),
     )
     if rc != 0:
         raise ValueError("oracle rejected the arguments")

@@ -31,11 +31,18 @@
  *    be written").
  *  - indexer_scores: groups are uniform, group g = rows [g*G, (g+1)*G) with
  *    G = rows / groups.
+ *  - NVFP4 indexer_scores ("flashinfer.sdsa.indexer_scores": the query,
+ *    key_cache, query_scales and key_scales parameters): element d of a
+ *    128-value row is the E2M1 code in byte d/2, low nibble for even d, high
+ *    nibble for odd d; its value is that code times the E4M3 scale number
+ *    d/16 of the row (query_scales [rows][8], key_scales [pages][64][8]).
+ *    No per-tensor scale appears in that call.
  *
  * Arithmetic: every product of two e4m3 values is a multiple of 2^-18 below
  * 2^18 in magnitude, and every product of two bf16 values has at most 16
  * significant bits, so the 128-term dot products are exact in fp64 in any
- * order.  The only roundings are the fp64 products w*relu(x), the fp64 sum
+ * order; so is an NVFP4 dot product, whose terms are products of four values
+ * of at most 4 significant bits each, between 2^-40 and 2^23.  The only roundings are the fp64 products w*relu(x), the fp64 sum
  * over heads and the final product with s_p.
  */
 #include <math.h>
@@ -68,6 +75,18 @@ double orc_e4m3_decode(uint8_t code)
         mag = ldexp((double)m, -9);             /* m/8 * 2^(1-7) */
     else
         mag = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* OCP 4-bit float E2M1: 1 sign bit (bit 3), 2 exponent bits with bias 1, 1
+ * mantissa bit.  Exponent field 0 encodes the subnormal m * 0.5; there are no
+ * infinities or NaNs, so the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_decode(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 0x3;
+    int m = code & 0x1;
+    double mag = e == 0 ? 0.5 * m : ldexp(1.0 + m / 2.0, e - 1);
     return sign ? -mag : mag;
 }
 
@@ -326,6 +345,117 @@ int orc_indexer_scores_bf16(const uint16_t* query, int rows, const uint8_t* key_
     J.max_context = max_context;
     pthread_mutex_init(&J.lock, NULL);
     orc_run_threads(orc_bf16_worker, &J, nthreads);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 indexer scores                                                */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    const uint8_t* query;          /* [rows][64] packed E2M1 */
+    const uint8_t* query_scales;   /* [rows][8] E4M3 */
+    int rows;
+    const uint8_t* key_cache;      /* page P at P * page_stride_bytes: [64][64] packed */
+    int64_t page_stride_bytes;
+    const uint8_t* key_scales;     /* page P at P * scale_page_stride_bytes: [64][8] E4M3 */
+    int64_t scale_page_stride_bytes;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    const int32_t* context_lengths;
+    const int32_t* requests;
+    int groups;
+    double* scores;
+    double* mag;
+    int64_t scores_stride;
+    int max_context;
+    int next_group;
+    double e2m1[16];
+    double e4m3[256];
+    pthread_mutex_t lock;
+} orc_nvfp4_job;
+
+/* Value of element d of a packed row with its eight per-16 scales. */
+static double orc_nvfp4_value(const orc_nvfp4_job* J, const uint8_t* packed,
+                              const uint8_t* scales, int d)
+{
+    const uint8_t byte = packed[d / 2];
+    const uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+    return J->e2m1[code] * J->e4m3[scales[d / 16]];
+}
+
+static void orc_nvfp4_group(orc_nvfp4_job* J, int g)
+{
+    const int G = J->rows / J->groups;
+    const int32_t len = J->context_lengths[g];
+    if (len <= 0) return;                           /* reads nothing, writes nothing */
+    const int32_t req = J->requests[g];
+    for (int r = g * G; r < (g + 1) * G; ++r) {
+        const uint8_t* qp = J->query + (int64_t)r * (ORC_HEAD_DIM / 2);
+        const uint8_t* qs = J->query_scales + (int64_t)r * (ORC_HEAD_DIM / 16);
+        for (int k = 0; k < len && k < J->max_context; ++k) {
+            const int64_t page = J->block_table[(int64_t)req * J->bt_stride + k / ORC_BLOCK_KEYS];
+            const int key = k % ORC_BLOCK_KEYS;
+            const uint8_t* kp = J->key_cache + page * J->page_stride_bytes +
+                                (int64_t)key * (ORC_HEAD_DIM / 2);
+            const uint8_t* ks = J->key_scales + page * J->scale_page_stride_bytes +
+                                (int64_t)key * (ORC_HEAD_DIM / 16);
+            double dot = 0.0, bound = 0.0;
+            for (int d = 0; d < ORC_HEAD_DIM; ++d) {
+                const double prod = orc_nvfp4_value(J, qp, qs, d) * orc_nvfp4_value(J, kp, ks, d);
+                dot += prod;
+                bound += fabs(prod);
+            }
+            J->scores[(int64_t)r * J->scores_stride + k] = dot;
+            if (J->mag) J->mag[(int64_t)r * J->scores_stride + k] = bound;
+        }
+    }
+}
+
+static void* orc_nvfp4_worker(void* arg)
+{
+    orc_nvfp4_job* J = (orc_nvfp4_job*)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int g = J->next_group++;
+        pthread_mutex_unlock(&J->lock);
+        if (g >= J->groups) break;
+        orc_nvfp4_group(J, g);
+    }
+    return NULL;
+}
+
+/* scores[r, k] = (dequantised query row r) . (dequantised key k of the
+ * group's request), in fp64, for every group g with context_lengths[g] > 0,
+ * rows r of group g and k < min(length, max_context); nothing else is
+ * written.  Dequantisation: element d = E2M1 code (byte d/2, low nibble for
+ * even d) times the row's E4M3 scale d/16.  If mag is not NULL it receives
+ * sum_d |q_d * k_d| at the same places.  Returns 0, or -1 on bad arguments. */
+int orc_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, int rows,
+                             const uint8_t* key_cache, int64_t page_stride_bytes,
+                             const uint8_t* key_scales, int64_t scale_page_stride_bytes,
+                             const int32_t* block_table, int64_t bt_stride,
+                             const int32_t* context_lengths, const int32_t* requests, int groups,
+                             double* scores, double* mag, int64_t scores_stride, int max_context,
+                             int nthreads)
+{
+    if (!query || !query_scales || !key_cache || !key_scales || !block_table ||
+        !context_lengths || !requests || !scores)
+        return -1;
+    if (groups <= 0 || rows % groups != 0) return -1;
+    orc_nvfp4_job J;
+    memset(&J, 0, sizeof J);
+    J.query = query; J.query_scales = query_scales; J.rows = rows;
+    J.key_cache = key_cache; J.page_stride_bytes = page_stride_bytes;
+    J.key_scales = key_scales; J.scale_page_stride_bytes = scale_page_stride_bytes;
+    J.block_table = block_table; J.bt_stride = bt_stride;
+    J.context_lengths = context_lengths; J.requests = requests; J.groups = groups;
+    J.scores = scores; J.mag = mag; J.scores_stride = scores_stride; J.max_context = max_context;
+    for (int c = 0; c < 16; ++c) J.e2m1[c] = orc_e2m1_decode((uint8_t)c);
+    for (int c = 0; c < 256; ++c) J.e4m3[c] = orc_e4m3_decode((uint8_t)c);
+    pthread_mutex_init(&J.lock, NULL);
+    orc_run_threads(orc_nvfp4_worker, &J, nthreads);
     pthread_mutex_destroy(&J.lock);
     return 0;
 }

@@ -316,3 +316,138 @@ def indexer(group_size: int, seed: int = 5, groups: int = 256, max_context: int 
     req[lens == 0] = np.int32(-123456789)
     return Bf16Problem(f"indexer_g{group_size}", seed, group_size, query, kc, stride, bt, lens,
                        req, max_context)
+
+
+# ---------------------------------------------------------------- NVFP4 indexer
+
+NVFP4_ROW_BYTES = HEAD_DIM // 2        # 64: two E2M1 codes per byte
+NVFP4_SCALES = HEAD_DIM // 16          # 8 E4M3 scales per row
+NVFP4_PAGE_KEY_BYTES = BLOCK_KEYS * NVFP4_ROW_BYTES    # 4096
+NVFP4_PAGE_SCALE_BYTES = BLOCK_KEYS * NVFP4_SCALES     # 512
+E4M3_NAN = 0x7F
+
+
+@dataclass
+class Nvfp4Problem:
+    """Single-head indexer problem over NVFP4 queries and keys.  Keys of page
+    P start at byte ``key_off + P*page_stride_bytes`` of ``key_buf`` (64 rows
+    of 64 packed bytes); their scales at ``scale_off + P*scale_page_stride_bytes``
+    of ``scale_buf`` (64 rows of 8 E4M3 bytes).  With ``fused`` the two are one
+    buffer holding each page's keys and then its scales."""
+    name: str
+    seed: int
+    group_size: int
+    query: np.ndarray            # uint8 [rows, 64]
+    query_scales: np.ndarray     # uint8 [rows, 8]
+    key_buf: np.ndarray          # uint8 flat
+    key_off: int
+    page_stride_bytes: int
+    scale_buf: np.ndarray        # uint8 flat (the same array as key_buf when fused)
+    scale_off: int
+    scale_page_stride_bytes: int
+    num_pages: int
+    block_table: np.ndarray      # int32 [requests, width]
+    context_lengths: np.ndarray  # int32 [groups]
+    requests: np.ndarray         # int32 [groups]
+    max_context: int
+    fused: bool = False
+
+    @property
+    def rows(self) -> int:
+        return int(self.query.shape[0])
+
+    @property
+    def groups(self) -> int:
+        return int(self.context_lengths.shape[0])
+
+    @property
+    def positions(self) -> int:
+        return int(np.maximum(self.context_lengths, 0).sum())
+
+    def key_view(self) -> np.ndarray:
+        return self.key_buf[self.key_off:]
+
+    def scale_view(self) -> np.ndarray:
+        return self.scale_buf[self.scale_off:]
+
+    def algorithmic_bytes(self) -> int:
+        G = self.group_size
+        total = self.rows * (NVFP4_ROW_BYTES + NVFP4_SCALES)
+        for L in self.context_lengths.tolist():
+            if L > 0:
+                total += L * (NVFP4_ROW_BYTES + NVFP4_SCALES) + G * L * 4 + blocks_for(L) * 4
+        return total
+
+    def algorithmic_flops(self) -> int:
+        return int(2 * HEAD_DIM * self.group_size * self.positions)
+
+
+def random_e4m3_scales(g: np.random.Generator, shape, lo_exp: int = -3, hi_exp: int = 3):
+    """Random positive normal E4M3 codes with exponents in [lo_exp, hi_exp]
+    (bias 7) and any mantissa: the bytes directly, no rounding involved."""
+    e = g.integers(lo_exp + 7, hi_exp + 7, size=shape, endpoint=True)
+    m = g.integers(0, 7, size=shape, endpoint=True)
+    return ((e << 3) | m).astype(np.uint8)
+
+
+def indexer_nvfp4(group_size: int, seed: int = 6, groups: int = 256, max_context: int = 65536,
+                  min_zero: int = 8, lo: int = 0, hi: int | None = None, fused: bool = True,
+                  page_pad_bytes: int = 0, scale_pad_bytes: int = 0,
+                  poison: bool = True) -> Nvfp4Problem:
+    """NVFP4 single-head problem: ``groups`` groups of ``group_size`` query rows,
+    one request each, lengths uniform on [lo, hi] with at least ``min_zero``
+    forced zeros.  E2M1 codes are uniform over all 16 values (bytes uniform on
+    0..255) and scales are random positive E4M3 codes between 2^-3 and 2^3.
+    ``fused``: one buffer of pages of [4096 key bytes][512 scale bytes]
+    (+ ``page_pad_bytes``); otherwise separate key and scale buffers, pages
+    4096 + ``page_pad_bytes`` and 512 + ``scale_pad_bytes`` bytes apart.  With
+    ``poison`` every pad byte and the spare page's scales are E4M3 NaN, so a
+    read outside a group's pages shows up as a NaN score."""
+    g = rng(seed)
+    hi = max_context if hi is None else hi
+    lens = g.integers(lo, hi, size=groups, endpoint=True).astype(np.int32)
+    if min_zero:
+        lens[g.choice(groups, size=min(min_zero, groups), replace=False)] = 0
+    rows = groups * group_size
+    need = np.array([blocks_for(L) for L in lens.tolist()], dtype=np.int64)
+    width = max(1, (max_context + BLOCK_KEYS - 1) // BLOCK_KEYS)
+    pool = int(need.sum())
+    perm = g.permutation(pool).astype(np.int32)
+    num_pages = pool + (1 if poison else 0)
+    bt = np.full((groups, width), pool if poison else 0, dtype=np.int32)
+    off = 0
+    for r in range(groups):
+        bt[r, :need[r]] = perm[off:off + need[r]]
+        off += int(need[r])
+    query = g.integers(0, 255, size=(rows, NVFP4_ROW_BYTES), endpoint=True).astype(np.uint8)
+    qscales = random_e4m3_scales(g, (rows, NVFP4_SCALES))
+    keys = g.integers(0, 255, size=(num_pages, NVFP4_PAGE_KEY_BYTES), endpoint=True).astype(np.uint8)
+    kscales = random_e4m3_scales(g, (num_pages, NVFP4_PAGE_SCALE_BYTES))
+    if poison:
+        kscales[pool:] = E4M3_NAN
+    fill = E4M3_NAN if poison else 0
+    if fused:
+        stride = NVFP4_PAGE_KEY_BYTES + NVFP4_PAGE_SCALE_BYTES + page_pad_bytes
+        assert stride % 16 == 0
+        buf = np.full((num_pages, stride), fill, dtype=np.uint8)
+        buf[:, :NVFP4_PAGE_KEY_BYTES] = keys
+        buf[:, NVFP4_PAGE_KEY_BYTES:NVFP4_PAGE_KEY_BYTES + NVFP4_PAGE_SCALE_BYTES] = kscales
+        flat = buf.reshape(-1)
+        p = Nvfp4Problem(f"nvfp4_g{group_size}", seed, group_size, query, qscales, flat, 0, stride,
+                         flat, NVFP4_PAGE_KEY_BYTES, stride, num_pages, bt, lens, None,
+                         max_context, fused=True)
+    else:
+        kstride = NVFP4_PAGE_KEY_BYTES + page_pad_bytes
+        sstride = NVFP4_PAGE_SCALE_BYTES + scale_pad_bytes
+        assert kstride % 16 == 0 and sstride % 8 == 0
+        kb = np.full((num_pages, kstride), fill, dtype=np.uint8)
+        kb[:, :NVFP4_PAGE_KEY_BYTES] = keys
+        sb = np.full((num_pages, sstride), fill, dtype=np.uint8)
+        sb[:, :NVFP4_PAGE_SCALE_BYTES] = kscales
+        p = Nvfp4Problem(f"nvfp4_g{group_size}", seed, group_size, query, qscales,
+                         kb.reshape(-1), 0, kstride, sb.reshape(-1), 0, sstride, num_pages, bt,
+                         lens, None, max_context, fused=False)
+    req = np.arange(groups, dtype=np.int32)
+    req[lens == 0] = np.int32(-123456789)     # a group of length 0 may name any request
+    p.requests = req
+    return p

@@ -2,7 +2,8 @@
 
 Each case plants one mistake in a copy of ``oracle/oracle.c`` (a dropped
 term, a wrong sign, index or operand), builds it with gcc on the CPU, and runs
-every pin in ``test_oracle_pins.py`` against it: at least one pin must fail.
+every pin in ``test_oracle_pins.py`` and ``test_oracle_nvfp4_pins.py``
+against it: at least one pin must fail.
 The oracle itself is never modified.
 """
 import inspect
@@ -13,6 +14,7 @@ from concurrent.futures import ThreadPoolExecutor
 import pytest
 
 import oracle
+from tests import test_oracle_nvfp4_pins as nvfp4_pins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -35,18 +37,31 @@ MUTANTS = {
                                 "J->block_table[p / ORC_BLOCK_KEYS]"),
     "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "e4m3_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
-    "bf16_page_stride_fixed": ("page * J->page_stride_bytes", "page * 16384"),
-    "bf16_group_rows": ("for (int r = g * G; r < (g + 1) * G; ++r)", "for (int r = g; r < g + G; ++r)"),
+    "bf16_page_stride_fixed": ("page * J->page_stride_bytes +\n                                (int64_t)(k % ORC_BLOCK_KEYS)",
+                               "page * 16384 +\n                                (int64_t)(k % ORC_BLOCK_KEYS)"),
+    "bf16_group_rows": ("for (int r = g * G; r < (g + 1) * G; ++r) {\n        const uint16_t* qr",
+                        "for (int r = g; r < g + G; ++r) {\n        const uint16_t* qr"),
+    "nvfp4_group_rows": ("for (int r = g * G; r < (g + 1) * G; ++r) {\n        const uint8_t* qp",
+                         "for (int r = g; r < g + G; ++r) {\n        const uint8_t* qp"),
     "bf16_key_stride": ("(int64_t)(k % ORC_BLOCK_KEYS) * ORC_HEAD_DIM * 2", "(int64_t)(k % ORC_BLOCK_KEYS) * ORC_HEAD_DIM"),
     "schedule_ceil_split": ("int64_t base = total / num_ctas, extra = total % num_ctas;",
                             "int64_t base = (total + num_ctas - 1) / num_ctas, extra = 0;"),
     "schedule_skips_empty_wrong": ("if (start < prefix + nb) break;", "if (start <= prefix + nb) break;"),
+    "nvfp4_scale_per_8": ("J->e4m3[scales[d / 16]]", "J->e4m3[scales[(d / 8) % 8]]"),
+    "nvfp4_key_scale_row": ("(int64_t)key * (ORC_HEAD_DIM / 16)", "(int64_t)key * (ORC_HEAD_DIM / 32)"),
+    "nvfp4_scale_stride_fixed": ("page * J->scale_page_stride_bytes", "page * 512"),
+    "nvfp4_query_scale_by_group": ("J->query_scales + (int64_t)r * (ORC_HEAD_DIM / 16)",
+                                   "J->query_scales + (int64_t)g * (ORC_HEAD_DIM / 16)"),
+    "e2m1_bias": ("ldexp(1.0 + m / 2.0, e - 1)", "ldexp(1.0 + m / 2.0, e)"),
+    "e2m1_subnormal": ("e == 0 ? 0.5 * m :", "e == 0 ? 1.0 * m :"),
 }
 
 
 def _pin_functions():
     out = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+    members = (inspect.getmembers(pins, inspect.isfunction) +
+               inspect.getmembers(nvfp4_pins, inspect.isfunction))
+    for name, fn in members:
         if not name.startswith("test_"):
             continue
         marks = getattr(fn, "pytestmark", [])
