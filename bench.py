@@ -42,6 +42,9 @@ WORKLOAD_TEXT = {
     "mtp4": "MTP verify: batch 32, next_n 4, 64 heads, seq_lens U[8192,65536], decode layout",
     "skewed": "skewed: 16 requests, next_n 1, 64 heads, one 131072, three empty, twelve "
               "U[512,4096]",
+    "nvfp4_g8": "single-head NVFP4 indexer_scores: 256 groups of 8 rows, E2M1 codes with E4M3 "
+                "scales per 16 values, pages of 4096 code bytes then 512 scale bytes, "
+                "context_lengths U[0,65536] (8 zeros), fp32 scores [2048, 65536]",
 }
 
 
@@ -62,6 +65,9 @@ def make_problem(workload: str, rank: int):
         return W.mtp(next_n=n, seed=(2 if n == 4 else 3) + off, poison=False)
     if workload == "skewed":
         return W.skewed(seed=4 + off)
+    if workload.startswith("nvfp4_g"):
+        return W.indexer_nvfp4(group_size=int(workload[len("nvfp4_g"):]), seed=6 + off,
+                               poison=False)
     if workload.startswith("indexer_g"):
         return W.indexer(group_size=int(workload[len("indexer_g"):]), seed=5 + off, poison=False)
     raise SystemExit(f"unknown workload {workload}")
@@ -312,6 +318,8 @@ def main():
     dev = torch.device("cuda", local_rank)
     p = make_problem(args.workload, rank)
     is_fp8 = hasattr(p, "next_n")
+    from sparse_attention_indexer_logits_gb300 import workloads as W
+    is_nvfp4 = isinstance(p, W.Nvfp4Problem)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     copies = args.copies if args.l2 == "rotate" else 1
@@ -328,6 +336,22 @@ def main():
             pml.pml_fp8_paged_mqa_logits_ex(d["q"], d["kv"], d["w"], d["sl"], d["bt"], d["out"],
                                             p.max_context, p.next_n, stream=stream)
         kernel = "fp8_logits_kernel"
+        bound_name = "hbm"
+    elif is_nvfp4:
+        def device_set():
+            kb = t(p.key_buf)
+            return dict(q=t(p.query), qs=t(p.query_scales), kb=kb,
+                        sb=kb if p.fused else t(p.scale_buf), bt=t(p.block_table),
+                        cl=t(p.context_lengths), rq=t(p.requests),
+                        out=torch.zeros((p.rows, p.max_context), dtype=torch.float32, device=dev))
+        sets = [device_set() for _ in range(copies)]
+
+        def step(d, stream=None):
+            pml.pml_indexer_scores_nvfp4(d["q"], d["qs"], d["kb"][p.key_off:], p.page_stride_bytes,
+                                         d["sb"][p.scale_off:], p.scale_page_stride_bytes,
+                                         p.num_pages, d["bt"], d["cl"], d["rq"], d["out"],
+                                         p.max_context, stream=stream)
+        kernel = "nvfp4_scores_kernel"
         bound_name = "hbm"
     else:
         def device_set():
@@ -403,6 +427,22 @@ def main():
                 d.copy_(h, non_blocking=True)
             step(d0)
             hout.copy_(d0["out"], non_blocking=True)
+    elif is_nvfp4:
+        d0 = sets[0]
+        bufs = [(d0["q"], p.query), (d0["qs"], p.query_scales), (d0["kb"], p.key_buf),
+                (d0["bt"], p.block_table), (d0["cl"], p.context_lengths), (d0["rq"], p.requests)]
+        if not p.fused:
+            bufs.append((d0["sb"], p.scale_buf))
+        inputs = tuple((d, torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) for d, a in bufs)
+        hout = torch.empty(d0["out"].shape, dtype=torch.float32).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for _, h in inputs)
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d, h in inputs:
+                d.copy_(h, non_blocking=True)
+            step(d0)
+            hout.copy_(d0["out"], non_blocking=True)
     else:
         hq = torch.from_numpy(p.query.view(np.int16)).pin_memory()
         hkc = torch.from_numpy(p.key_cache).pin_memory()
@@ -450,7 +490,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": (("e4m3 x e4m3 -> f32" + (" -> bf16 out" if out_dtype == torch.bfloat16 else ""))
-                      if is_fp8 else "bf16 x bf16 -> f32"),
+                      if is_fp8 else ("nvfp4 (e2m1 x e4m3/16) -> f16 x f16 -> f32" if is_nvfp4
+                                      else "bf16 x bf16 -> f32")),
             "data": "synthetic (seeded generators; no public dataset on the pages)",
             "config": dict(config_of(args.workload, p, world, args.l2, copies),
                            **({"output_dtype": args.out_dtype} if is_fp8 else {})),

@@ -184,6 +184,40 @@ int pml_indexer_scores_bf16(const uint16_t* query, int rows, const uint16_t* key
                             float* scores, int64_t scores_stride, int max_context, void* stream);
 
 /*
+ * pml_indexer_scores_nvfp4 ("flashinfer.sdsa.indexer_scores": the NVFP4 forms
+ * of query, key_cache, query_scales and key_scales).
+ *
+ *   scores[r, k] = q_r . k_k       (dequantised values; one head, no weight,
+ *                                   no rectifier)
+ *
+ * A row of 128 values is 64 bytes of E2M1 codes, two to a byte (element d in
+ * byte d/2; the low nibble holds the even element), and 8 E4M3 scale codes,
+ * scale j applying to elements 16j .. 16j+15: value = E2M1(code) * E4M3(scale).
+ * Groups, lengths, requests, the written region and the status bits are
+ * those of pml_indexer_scores_bf16.
+ *
+ * query           uint8 [rows, 64], 16-byte aligned
+ * query_scales    uint8 [rows, 8] (E4M3), 8-byte aligned
+ * key_cache       page P's 64 keys x 64 bytes start at byte P*page_stride_bytes;
+ *                 base 16-byte aligned, page_stride_bytes a multiple of 16 and
+ *                 >= 4096
+ * key_scales      page P's 64 keys x 8 scale bytes start at byte
+ *                 P*scale_page_stride_bytes; base 8-byte aligned,
+ *                 scale_page_stride_bytes a multiple of 8 and >= 512 (the two
+ *                 may be views of one cache holding each page's keys and then
+ *                 its scales)
+ * num_pages       pages in both (block_table entries must be below it)
+ * scores          fp32 [rows, scores_stride], scores_stride >= max_context
+ */
+int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, int rows,
+                             const uint8_t* key_cache, int64_t page_stride_bytes,
+                             const uint8_t* key_scales, int64_t scale_page_stride_bytes,
+                             int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                             int num_requests, const int32_t* context_lengths,
+                             const int32_t* requests, int groups, float* scores,
+                             int64_t scores_stride, int max_context, void* stream);
+
+/*
  * pml_fp8_paged_mqa_logits_noalloc -- the two-step call (pml_schedule, then
  * pml_fp8_paged_mqa_logits with that schedule) for callers that cannot
  * allocate device memory.  The documentation pages have no counterpart: it

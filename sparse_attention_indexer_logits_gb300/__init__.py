@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
   option (fp32 or bf16 logits).
 * ``pml_indexer_scores_bf16`` -- the single-head bf16 case
   ("flashinfer.sdsa.indexer_scores").
+* ``pml_indexer_scores_nvfp4`` -- the same over NVFP4 queries and keys.
 
 ``fp8_paged_mqa_logits`` / ``indexer_scores`` wrap them with the pages'
 keyword style (``out=``, ``schedule_meta=``, ``scores=``).
@@ -30,7 +31,8 @@ import torch
 __all__ = [
     "PmlError", "lib", "library_path", "pml_schedule", "pml_fp8_paged_mqa_logits",
     "pml_fp8_paged_mqa_logits_ex",
-    "pml_indexer_scores_bf16", "pml_fp8_paged_mqa_logits_noalloc", "pml_device_status",
+    "pml_indexer_scores_bf16", "pml_indexer_scores_nvfp4", "pml_fp8_paged_mqa_logits_noalloc",
+    "pml_device_status",
     "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
     "fp8_paged_mqa_logits", "indexer_scores", "compute_paged_mqa_logits_schedule",
 ]
@@ -84,6 +86,9 @@ def lib() -> ctypes.CDLL:
         L.pml_indexer_scores_bf16.argtypes = [P, i32, P, i64, i64, P, i64, i32, P, P, i32, P, i64,
                                               i32, P]
         L.pml_indexer_scores_bf16.restype = i32
+        L.pml_indexer_scores_nvfp4.argtypes = [P, P, i32, P, i64, P, i64, i64, P, i64, i32, P, P,
+                                               i32, P, i64, i32, P]
+        L.pml_indexer_scores_nvfp4.restype = i32
         L.pml_fp8_paged_mqa_logits_noalloc.argtypes = [P, P, i64, P, P, P, i64, i32, P, i64, i32,
                                                        i32, i32, i32, P]
         L.pml_fp8_paged_mqa_logits_noalloc.restype = i32
@@ -261,6 +266,41 @@ def pml_indexer_scores_bf16(query: torch.Tensor, key_cache: torch.Tensor, page_s
         _ptr(block_table), block_table.stride(0), block_table.shape[0], _ptr(context_lengths),
         _ptr(requests), context_lengths.numel(), _ptr(scores), scores.stride(0), max_context,
         _stream(stream)), "pml_indexer_scores_bf16")
+    return scores
+
+
+def pml_indexer_scores_nvfp4(query: torch.Tensor, query_scales: torch.Tensor,
+                             key_cache: torch.Tensor, page_stride_bytes: int,
+                             key_scales: torch.Tensor, scale_page_stride_bytes: int,
+                             num_pages: int, block_table: torch.Tensor,
+                             context_lengths: torch.Tensor, requests: torch.Tensor,
+                             scores: torch.Tensor, max_context: int, stream=None) -> torch.Tensor:
+    """``scores[r, k] = query[r] . key_k`` over NVFP4 rows: 64 bytes of E2M1
+    codes (two to a byte) and 8 E4M3 scales per row, one per 16 values.
+
+    query uint8 ``[rows, 64]``, query_scales uint8 ``[rows, 8]``; key_cache /
+    key_scales: CUDA tensors whose storage holds ``num_pages`` pages of 64x64
+    code bytes ``page_stride_bytes`` apart and of 64x8 scale bytes
+    ``scale_page_stride_bytes`` apart (they may view one buffer); the rest as
+    ``pml_indexer_scores_bf16``."""
+    for t, nm in ((query, "query"), (query_scales, "query_scales"), (context_lengths, "context_lengths"),
+                  (requests, "requests")):
+        _cuda(t, nm)
+    for t, nm in ((key_cache, "key_cache"), (key_scales, "key_scales"), (block_table, "block_table"),
+                  (scores, "scores")):
+        _cuda(t, nm, contiguous=False)
+    if query.element_size() != 1 or query.dim() != 2 or query.shape[1] != 64:
+        raise ValueError("query must be uint8 [rows, 64]")
+    if query_scales.element_size() != 1 or tuple(query_scales.shape) != (query.shape[0], 8):
+        raise ValueError("query_scales must be uint8 [rows, 8]")
+    if scores.dtype != torch.float32 or scores.stride(-1) != 1 or block_table.stride(-1) != 1:
+        raise ValueError("scores must be float32 with unit last stride; block_table unit stride")
+    _check(lib().pml_indexer_scores_nvfp4(
+        _ptr(query), _ptr(query_scales), query.shape[0], _ptr(key_cache), int(page_stride_bytes),
+        _ptr(key_scales), int(scale_page_stride_bytes), int(num_pages), _ptr(block_table),
+        block_table.stride(0), block_table.shape[0], _ptr(context_lengths), _ptr(requests),
+        context_lengths.numel(), _ptr(scores), scores.stride(0), max_context, _stream(stream)),
+        "pml_indexer_scores_nvfp4")
     return scores
 
 

@@ -18,6 +18,7 @@ using namespace pml;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxFp8Stages = 12;
 constexpr int kMaxBf16Stages = 8;
+constexpr int kMaxNvfp4Stages = 8;
 
 thread_local int g_last_cuda_error = 0;
 
@@ -236,6 +237,66 @@ int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64
         if (e != cudaSuccess) return cuda_fail(e);
     }
     e = launch_fp8_logits(num_heads, kmap, qmap, a, num_ctas, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PML_OK : cuda_fail(e);
+}
+
+int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, int rows,
+                             const uint8_t* key_cache, int64_t page_stride_bytes,
+                             const uint8_t* key_scales, int64_t scale_page_stride_bytes,
+                             int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                             int num_requests, const int32_t* context_lengths,
+                             const int32_t* requests, int groups, float* scores,
+                             int64_t scores_stride, int max_context, void* stream)
+{
+    if (rows < 0 || groups < 0) return PML_ERR_INVALID_ARG;
+    if (groups == 0) return rows == 0 ? PML_OK : PML_ERR_INVALID_ARG;
+    if (rows % groups != 0) return PML_ERR_INVALID_ARG;
+    const int G = rows / groups;
+    if (G < 1 || G > 8) return PML_ERR_UNSUPPORTED;
+    if (!query || !query_scales || !key_cache || !key_scales || !block_table ||
+        !context_lengths || !requests || !scores)
+        return PML_ERR_INVALID_ARG;
+    if (num_pages < 1 || num_pages > 0x7fffffffLL || num_requests < 1) return PML_ERR_INVALID_ARG;
+    if (page_stride_bytes < (int64_t)kBlockKeys * kHeadDim / 2) return PML_ERR_INVALID_ARG;
+    if (scale_page_stride_bytes < (int64_t)kBlockKeys * kHeadDim / 16) return PML_ERR_INVALID_ARG;
+    if (page_stride_bytes % 16 != 0 || scale_page_stride_bytes % 8 != 0) return PML_ERR_ALIGNMENT;
+    if (max_context < 1 || scores_stride < max_context) return PML_ERR_INVALID_ARG;
+    if (bt_stride < pml_min_block_table_width(max_context)) return PML_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(query_scales, 8) || !aligned(key_cache, 16) ||
+        !aligned(key_scales, 8) || !aligned(scores, 4) || !aligned(block_table, 4) ||
+        !aligned(context_lengths, 4) || !aligned(requests, 4))
+        return PML_ERR_ALIGNMENT;
+
+    DeviceInfo dev;
+    cudaError_t e = device_info(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    Nvfp4Args a;
+    a.query = query;
+    a.query_scales = query_scales;
+    a.key_cache = key_cache;
+    a.key_scales = key_scales;
+    a.context_lengths = context_lengths;
+    a.requests = requests;
+    a.block_table = block_table;
+    a.scores = scores;
+    a.status = dev.status;
+    a.page_stride = page_stride_bytes;
+    a.scale_stride = scale_page_stride_bytes;
+    a.bt_stride = bt_stride;
+    a.scores_stride = scores_stride;
+    a.num_pages = num_pages;
+    a.num_requests = num_requests;
+    a.groups = groups;
+    a.group_size = G;
+    a.max_context = max_context;
+    const size_t fixed = nvfp4_smem_bytes(0);
+    const size_t per_stage = nvfp4_smem_bytes(1) - fixed;
+    int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
+    if (stages > kMaxNvfp4Stages) stages = kMaxNvfp4Stages;
+    if (stages < 2) return PML_ERR_UNSUPPORTED;
+    a.stages = stages;
+    e = launch_nvfp4_scores(a, dev.sm_count, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 

@@ -44,14 +44,38 @@ struct Bf16Args {
     int q_box_rows;
 };
 
+struct Nvfp4Args {
+    const uint8_t* query;          // [rows][64] packed E2M1
+    const uint8_t* query_scales;   // [rows][8] E4M3
+    const uint8_t* key_cache;      // page P at P * page_stride: [64][64] packed E2M1
+    const uint8_t* key_scales;     // page P at P * scale_stride: [64][8] E4M3
+    const int32_t* context_lengths;
+    const int32_t* requests;
+    const int32_t* block_table;
+    float* scores;
+    unsigned int* status;
+    long long page_stride;
+    long long scale_stride;
+    long long bt_stride;
+    long long scores_stride;
+    long long num_pages;
+    int num_requests;
+    int groups;
+    int group_size;
+    int max_context;
+    int stages;
+};
+
 // Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
 size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
+size_t nvfp4_smem_bytes(int stages);
 
 cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
                               const Fp8Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
                                const Bf16Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
                             cudaStream_t stream);
 

@@ -1,0 +1,401 @@
+// Single-head NVFP4 indexer scores on sm_103a.
+//
+//   scores[r, k] = query[r] . key_k     for k < min(context_lengths[g], max_context)
+//
+// ("flashinfer.sdsa.indexer_scores": the NVFP4 forms of query [rows, 64] and
+// key_cache [pages, 64, 64] -- E2M1 values two to a byte -- with E4M3
+// query_scales [rows, 8] and key_scales [pages, 64, 8], one scale per 16
+// values; key pages any multiple of 16 bytes apart, scale pages any multiple
+// of 8; a score is the plain dot product of the dequantised query row and
+// key.)
+//
+// The bf16 engine with a dequantising stage in front of the tensor cores.  A
+// value is an E2M1 code (at most 2 significant bits) times an E4M3 scale (at
+// most 4), so it has at most 6 significant bits and |v| <= 6 * 448 = 2688:
+// exact in f16.  Each tile of two 64-key pages therefore becomes an f16
+// operand with no rounding, and tcgen05.mma kind::f16 accumulates the exact
+// f16 products in fp32.
+//
+//   warp 0     producer: per tile one bulk copy per 4 KB page of packed keys
+//              and 8-byte cp.async copies of the 64 x 8 scale bytes (their
+//              pages need only 8-byte alignment), all completing on the
+//              stage's `full` barrier.
+//   warp 1     MMA issue: 2 K-halves x 4 tcgen05.mma (K = 16) per tile
+//              against the group's rows (padded to N = 16), one commit.
+//   warps 2-5  epilogue: one key per thread, up to 8 scores per key.
+//   warps 6-9  dequantisation: thread t expands key row t of the tile --
+//              eight groups of 16 codes, cvt.rn.f16x2.e2m1x2 per byte pair
+//              and one f16x2 multiply by the group's scale -- into the
+//              128-byte-swizzled K-major layout the MMA reads (two K-halves
+//              of 64 values); per group of query rows, the same for the rows
+//              into one of two Q slots.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pml {
+
+namespace {
+
+constexpr int kN = 16;                                   // MMA N: group rows padded
+constexpr int kPackedRow = kHeadDim / 2;                 // 64 bytes of codes per row
+constexpr int kScalesPerRow = kHeadDim / 16;             // 8
+constexpr int kPackedPage = kBlockKeys * kPackedRow;     // 4096
+constexpr int kScalePage = kBlockKeys * kScalesPerRow;   // 512
+constexpr int kHalfBytes = kTileKeys * 128;              // 16 KB: one f16 K-half of a tile
+constexpr int kTileBytes = 2 * kHalfBytes;               // 32 KB
+constexpr int kPageHalfBytes = kBlockKeys * 128;         // 8 KB
+constexpr int kQHalfBytes = kN * 128;                    // 2 KB
+constexpr int kQSlotBytes = 2 * kQHalfBytes;             // 4 KB
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstEpiWarp = 2;
+constexpr int kFirstDeqWarp = 6;
+constexpr int kThreads = 320;
+
+struct Nvfp4Layout {
+    uint32_t tile, packed, scales, q, bar, misc, total;
+};
+
+__host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages)
+{
+    Nvfp4Layout L;
+    L.tile = 0;
+    L.packed = L.tile + (uint32_t)stages * kTileBytes;
+    L.scales = L.packed + (uint32_t)stages * 2 * kPackedPage;
+    L.q = L.scales + (uint32_t)stages * 2 * kScalePage;
+    L.bar = L.q + 2 * kQSlotBytes;
+    L.misc = L.bar + (uint32_t)(3 * stages + 8) * 8;
+    L.total = L.misc + 64;
+    return L;
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
+// K-major region whose rows are 128 bytes (8-row atoms of 1 KB).
+__device__ __forceinline__ uint32_t sw128(int r, int c)
+{
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Dequantise one 128-value row: 64 packed bytes and 8 scale codes -> f16,
+// written as 16 chunks of 16 bytes: chunk j of K-half h at half_base[h] +
+// sw128(row, j).
+__device__ __forceinline__ void dequant_row(const uint4 (&packed)[4], uint2 scales,
+                                            uint32_t half0, uint32_t half1, int row)
+{
+    const uint32_t sc[2] = {scales.x, scales.y};
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {                 // group of 16 values: 8 packed bytes
+        const uint4 v = packed[g / 2];
+        const uint32_t w0 = (g & 1) ? v.z : v.x;  // bytes 8g .. 8g+3
+        const uint32_t w1 = (g & 1) ? v.w : v.y;  // bytes 8g+4 .. 8g+7
+        const uint32_t s2 = e4m3_to_f16x2_dup((sc[g / 4] >> (8 * (g % 4))) & 0xFF);
+        uint32_t h[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            h[b] = mul_f16x2(e2m1x2_to_f16x2((w0 >> (8 * b)) & 0xFF), s2);
+            h[4 + b] = mul_f16x2(e2m1x2_to_f16x2((w1 >> (8 * b)) & 0xFF), s2);
+        }
+        const uint32_t base = (g < 4) ? half0 : half1;
+        const int c = (g % 4) * 2;                // two 16-byte chunks per group
+        st_shared_v4(base + sw128(row, c), h[0], h[1], h[2], h[3]);
+        st_shared_v4(base + sw128(row, c + 1), h[4], h[5], h[6], h[7]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int S = a.stages;
+    const int G = a.group_size;
+    const Nvfp4Layout L = nvfp4_layout(S);
+
+    const uint32_t base = smem_addr(smem);
+    const uint32_t tile_base = base + L.tile;
+    const uint32_t packed_base = base + L.packed;
+    const uint32_t scale_base = base + L.scales;
+    const uint32_t q_base = base + L.q;
+    const uint32_t bar = base + L.bar;
+    auto full_bar = [&](int s) { return bar + 8u * s; };
+    auto deq_bar = [&](int s) { return bar + 8u * (S + s); };
+    auto empty_bar = [&](int s) { return bar + 8u * (2 * S + s); };
+    const uint32_t tfull_bar0 = bar + 8u * (3 * S);
+    const uint32_t tempty_bar0 = bar + 8u * (3 * S + 2);
+    const uint32_t qfull_bar0 = bar + 8u * (3 * S + 4);
+    const uint32_t qempty_bar0 = bar + 8u * (3 * S + 6);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+    int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kTmemCols = 32;    // two accumulators of N = 16 columns
+
+    if (warp == kProducerWarp) {
+        const long long total = warp_total_blocks(a.context_lengths, a.groups);
+        const long long s0 = range_start(total, gridDim.x, blockIdx.x);
+        const long long s1 = range_start(total, gridDim.x, blockIdx.x + 1);
+        int sb, sj, eb, ej;
+        warp_locate2(a.context_lengths, a.groups, s0, s1, sb, sj, eb, ej);
+        if (lane == 0) {
+            sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
+            *abort_flag = 0;
+            for (int s = 0; s < S; ++s) {
+                mbar_init(full_bar(s), 1 + 32);   // expect_tx arrive + each lane's cp.async
+                mbar_init(deq_bar(s), 4);
+                mbar_init(empty_bar(s), 4);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(tfull_bar0 + 8u * i, 1);
+                mbar_init(tempty_bar0 + 8u * i, 4);
+                mbar_init(qfull_bar0 + 8u * i, 4);
+                mbar_init(qempty_bar0 + 8u * i, 4);
+            }
+            fence_mbar_init();
+        }
+    } else if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int sb = sched[0], sj = sched[1], eb = sched[2], ej = sched[3];
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        const uint64_t policy = policy_evict_first();
+        Walk w;
+        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+        int it = 0, prev_g = -1;
+        long long bt_row = 0;
+        bool ok = true;
+        while (!w.done()) {
+            const int c = w.cnt();
+            if (w.b != prev_g) {
+                int req = __ldg(a.requests + w.b);
+                if (req < 0 || req >= a.num_requests) {
+                    if (lane == 0) atomicOr(a.status, kStatusBadRequest);
+                    req = 0;
+                }
+                bt_row = (long long)req * a.bt_stride;
+                prev_g = w.b;
+            }
+            const int s = it % S;
+            if (lane == 0) ok = mbar_wait(empty_bar(s), ((it / S) & 1) ^ 1, abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            long long page[2] = {0, 0};
+            int nload = 0;
+            for (int cc = 0; cc < c; ++cc) {
+                if ((long long)(w.j + cc) * kBlockKeys < a.max_context) {
+                    long long pg = __ldg(a.block_table + bt_row + w.j + cc);
+                    if (pg < 0 || pg >= a.num_pages) {
+                        if (lane == 0) atomicOr(a.status, kStatusBadBlock);
+                        pg = 0;
+                    }
+                    page[cc] = pg;
+                    nload = cc + 1;
+                }
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kPackedPage);
+                for (int cc = 0; cc < nload; ++cc)
+                    bulk_load_stream(packed_base + (uint32_t)(2 * s + cc) * kPackedPage,
+                                     a.key_cache + page[cc] * a.page_stride, kPackedPage,
+                                     full_bar(s), policy);
+            }
+            for (int cc = 0; cc < nload; ++cc) {
+                const uint8_t* src = a.key_scales + page[cc] * a.scale_stride;
+                const uint32_t dst = scale_base + (uint32_t)(2 * s + cc) * kScalePage;
+                cp_async8(dst + lane * 8, src + lane * 8);
+                cp_async8(dst + (lane + 32) * 8, src + (lane + 32) * 8);
+            }
+            cp_async_arrive(full_bar(s));
+            w.advance(c);
+            ++it;
+        }
+        if (!ok && lane == 0) {
+            for (int t = (it > S ? it - S : 0); t < it; ++t)
+                mbar_wait_drain(full_bar(t % S), (t / S) & 1);
+        }
+        cp_async_wait_all();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        const uint32_t idesc = make_idesc(0, 0, kTileKeys, kN);   // f16 x f16 -> f32
+        Walk w;
+        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+        int it = 0, qcount = 0, prev_g = -1, slot = 0;
+        bool ok = true;
+        while (!w.done()) {
+            const int c = w.cnt();
+            if (w.b != prev_g) {
+                slot = qcount & 1;
+                ok = mbar_wait(qfull_bar0 + 8u * slot, (qcount >> 1) & 1, abort_flag, a.status);
+                if (!ok) break;
+                ++qcount;
+                prev_g = w.b;
+            }
+            const int s = it % S;
+            ok = mbar_wait(deq_bar(s), (it / S) & 1, abort_flag, a.status);
+            if (!ok) break;
+            const int acc = it & 1;
+            ok = mbar_wait(tempty_bar0 + 8u * acc, ((it >> 1) & 1) ^ 1, abort_flag, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d = tmem_base + (uint32_t)(acc * kN);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t ad = smem_desc_sw128(tile_base + s * kTileBytes + h * kHalfBytes);
+                    const uint64_t bd = smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (h | k) ? 1u : 0u);
+                }
+                mma_commit(tfull_bar0 + 8u * acc);
+            }
+            __syncwarp();
+            w.advance(c);
+            ++it;
+        }
+        if (!ok && it > 0) mbar_wait_drain(tfull_bar0 + 8u * ((it - 1) & 1), ((it - 1) >> 1) & 1);
+    } else if (warp >= kFirstEpiWarp && warp < kFirstDeqWarp) {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int pg = row >> 6;
+        const int key = row & 63;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+        Walk w;
+        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+        int it = 0, qcount = 0, prev_g = -1, slot = 0, len = 0;
+        bool ok = true;
+        while (!w.done()) {
+            const int c = w.cnt();
+            if (w.b != prev_g) {
+                slot = qcount & 1;
+                ++qcount;
+                prev_g = w.b;
+                len = min(__ldg(a.context_lengths + w.b), a.max_context);
+            }
+            const bool last = w.last_of_request(c);
+            const int s = it % S;
+            const int acc = it & 1;
+            ok = mbar_wait(tfull_bar0 + 8u * acc, (it >> 1) & 1, abort_flag, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            float v[8];
+            tmem_ld8(lane_addr + (uint32_t)(acc * kN), v);
+            const int pos = (w.j + pg) * kBlockKeys + key;
+            if (pg < c && pos < len) {
+                float* dst = a.scores + (long long)w.b * G * a.scores_stride + pos;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < G) dst[(long long)r * a.scores_stride] = v[r];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(tempty_bar0 + 8u * acc);
+                mbar_arrive(empty_bar(s));
+                if (last) mbar_arrive(qempty_bar0 + 8u * slot);
+            }
+            w.advance(c);
+            ++it;
+        }
+    } else {
+        // ------------------------------------------------------------ dequantisation
+        const int t = threadIdx.x - 32 * kFirstDeqWarp;   // key row of the tile, 0..127
+        Walk w;
+        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+        int it = 0, qcount = 0, prev_g = -1;
+        bool ok = true;
+        while (!w.done()) {
+            const int c = w.cnt();
+            if (w.b != prev_g) {
+                // the group's query rows into the next Q slot (rows G..15 zero)
+                const int slot = qcount & 1;
+                ok = mbar_wait(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1, abort_flag,
+                               a.status);
+                if (!ok) break;
+                const uint32_t qh0 = q_base + slot * kQSlotBytes;
+                if (t < G) {
+                    const long long qrow = (long long)w.b * G + t;
+                    const uint4* src = reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
+                    const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
+                    const uint2 sc =
+                        __ldg(reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
+                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t);
+                } else if (t < kN) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        st_shared_v4(qh0 + sw128(t, ch), 0u, 0u, 0u, 0u);
+                        st_shared_v4(qh0 + kQHalfBytes + sw128(t, ch), 0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
+                ++qcount;
+                prev_g = w.b;
+            }
+            const int s = it % S;
+            ok = mbar_wait(full_bar(s), (it / S) & 1, abort_flag, a.status);
+            if (!ok) break;
+            const int pg = t >> 6, r = t & 63;
+            if (pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    smem + L.packed + (2 * s + pg) * kPackedPage + r * kPackedRow);
+                const uint4 pk[4] = {src[0], src[1], src[2], src[3]};
+                const uint2 sc = *reinterpret_cast<const uint2*>(
+                    smem + L.scales + (2 * s + pg) * kScalePage + r * kScalesPerRow);
+                const uint32_t h0 = tile_base + s * kTileBytes + pg * kPageHalfBytes;
+                dequant_row(pk, sc, h0, h0 + kHalfBytes, r);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(deq_bar(s));
+            w.advance(c);
+            ++it;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t nvfp4_smem_bytes(int stages) { return (size_t)nvfp4_layout(stages).total + 1024; }
+
+cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream)
+{
+    const size_t smem = nvfp4_smem_bytes(a.stages);
+    static int configured_device = -1;
+    static size_t configured_smem = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev || configured_smem < smem) {
+        e = cudaFuncSetAttribute(nvfp4_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+        configured_smem = smem;
+    }
+    nvfp4_scores_kernel<<<num_ctas, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pml

@@ -460,6 +460,59 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
                  : "memory");
 }
 
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// One arrival on the mbarrier once every cp.async this thread issued so far
+// has landed (the barrier's expected count includes it: noinc).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Two E2M1 codes (low nibble -> low half) to an f16x2, exactly.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
+{
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h)
+        : "r"(byte));
+    return h;
+}
+
+// An E4M3 code to an f16x2 holding its value twice, exactly.
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(code | (code << 8))));
+    return h;
+}
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Waits for every cp.async this thread issued.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+                 "r"(w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");

@@ -118,6 +118,30 @@ def test_bf16_argument_checks(L):
     assert _bf16(L, kc=P + 8) == 3
 
 
+def _nvfp4(L, **over):
+    a = dict(q=P, qs=P, rows=8, kc=P, stride=4096, ks=P, sstride=512, pages=4, bt=P,
+             bt_stride=4, nreq=2, cl=P, req=P, groups=2, sc=P, sc_stride=256, mc=256)
+    a.update(over)
+    return L.pml_indexer_scores_nvfp4(a["q"], a["qs"], a["rows"], a["kc"], a["stride"], a["ks"],
+                                      a["sstride"], a["pages"], a["bt"], a["bt_stride"], a["nreq"],
+                                      a["cl"], a["req"], a["groups"], a["sc"], a["sc_stride"],
+                                      a["mc"], None)
+
+
+def test_nvfp4_argument_checks(L):
+    assert _nvfp4(L, rows=0, groups=0) == 0
+    assert _nvfp4(L, rows=9) == 1                     # rows not a multiple of groups
+    assert _nvfp4(L, rows=18) == 2                    # group of 9 rows
+    assert _nvfp4(L, qs=None) == 1 and _nvfp4(L, ks=None) == 1
+    assert _nvfp4(L, stride=4096 + 8) == 3            # key pages a multiple of 16 apart
+    assert _nvfp4(L, sstride=512 + 4) == 3            # scale pages a multiple of 8 apart
+    assert _nvfp4(L, stride=2048) == 1                # key pages would overlap
+    assert _nvfp4(L, sstride=256) == 1                # scale pages would overlap
+    assert _nvfp4(L, q=P + 8) == 3 and _nvfp4(L, qs=P + 4) == 3
+    assert _nvfp4(L, kc=P + 8) == 3 and _nvfp4(L, ks=P + 4) == 3
+    assert _nvfp4(L, sc_stride=100) == 1 and _nvfp4(L, bt_stride=2) == 1
+
+
 def test_schedule_argument_checks(L):
     assert L.pml_schedule(P, 4, 1, 0, P, None) == 1
     assert L.pml_schedule(P, 4, 1, 8, None, None) == 1
