@@ -63,13 +63,14 @@ struct Nvfp4Args {
     int groups;
     int group_size;
     int max_context;
-    int stages;
+    int stages;      // staging slots (packed pages and scales of one tile)
+    int tiles;       // f16 tiles the MMA reads
 };
 
 // Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
 size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
-size_t nvfp4_smem_bytes(int stages);
+size_t nvfp4_smem_bytes(int stages, int tiles);
 
 cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
                               const Fp8Args& a, int num_ctas, cudaStream_t stream);

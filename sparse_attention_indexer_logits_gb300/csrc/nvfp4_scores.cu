@@ -19,9 +19,13 @@
 //   warp 0     producer: per tile one bulk copy per 4 KB page of packed keys
 //              and 8-byte cp.async copies of the 64 x 8 scale bytes (their
 //              pages need only 8-byte alignment), all completing on the
-//              stage's `full` barrier.
+//              staging slot's `full` barrier.  Staging slots (9 KB) are many
+//              and are freed as soon as the dequantising warps have read
+//              them; the f16 tiles (32 KB) are few and are freed by the MMA's
+//              commit, so most of the shared memory holds copies in flight.
 //   warp 1     MMA issue: 2 K-halves x 4 tcgen05.mma (K = 16) per tile
-//              against the group's rows (padded to N = 16), one commit.
+//              against the group's rows (padded to N = 16), one commit, into
+//              one of eight TMEM accumulators (16 columns each).
 //   warps 2-5  epilogue: one key per thread, up to 8 scores per key.
 //   warps 6-9  dequantisation: thread t expands key row t of the tile --
 //              eight groups of 16 codes, cvt.rn.f16x2.e2m1x2 per byte pair
@@ -56,19 +60,22 @@ constexpr int kFirstEpiWarp = 2;
 constexpr int kFirstDeqWarp = 6;
 constexpr int kThreads = 320;
 
+// Two rings: `stages` staging slots of one tile's packed pages and scale bytes
+// (what HBM delivers; deep, so that many copies are in flight) and `tiles`
+// f16 tiles (what the MMA reads; short-lived: freed by the MMA's commit).
 struct Nvfp4Layout {
     uint32_t tile, packed, scales, q, bar, misc, total;
 };
 
-__host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages)
+__host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages, int tiles)
 {
     Nvfp4Layout L;
     L.tile = 0;
-    L.packed = L.tile + (uint32_t)stages * kTileBytes;
+    L.packed = L.tile + (uint32_t)tiles * kTileBytes;
     L.scales = L.packed + (uint32_t)stages * 2 * kPackedPage;
     L.q = L.scales + (uint32_t)stages * 2 * kScalePage;
     L.bar = L.q + 2 * kQSlotBytes;
-    L.misc = L.bar + (uint32_t)(3 * stages + 8) * 8;
+    L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 20) * 8;
     L.total = L.misc + 64;
     return L;
 }
@@ -80,29 +87,40 @@ __device__ __forceinline__ uint32_t sw128(int r, int c)
     return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Dequantise one 128-value row: 64 packed bytes and 8 scale codes -> f16,
-// written as 16 chunks of 16 bytes: chunk j of K-half h at half_base[h] +
-// sw128(row, j).
-__device__ __forceinline__ void dequant_row(const uint4 (&packed)[4], uint2 scales,
-                                            uint32_t half0, uint32_t half1, int row)
+// Dequantise the 16 values of group g (8 packed bytes w0, w1) with scale code
+// sc into chunks 2(g%4), 2(g%4)+1 of row `row` of K-half g/4.
+__device__ __forceinline__ void dequant_group(uint32_t w0, uint32_t w1, uint32_t sc, int g,
+                                              uint32_t half0, uint32_t half1, int row)
 {
-    const uint32_t sc[2] = {scales.x, scales.y};
+    const uint32_t s2 = e4m3_to_f16x2_dup(sc);
+    uint32_t lo[4], hi[4], h[8];
+    e2m1x8_to_f16x2x4(w0, lo);
+    e2m1x8_to_f16x2x4(w1, hi);
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {                 // group of 16 values: 8 packed bytes
-        const uint4 v = packed[g / 2];
-        const uint32_t w0 = (g & 1) ? v.z : v.x;  // bytes 8g .. 8g+3
-        const uint32_t w1 = (g & 1) ? v.w : v.y;  // bytes 8g+4 .. 8g+7
-        const uint32_t s2 = e4m3_to_f16x2_dup((sc[g / 4] >> (8 * (g % 4))) & 0xFF);
-        uint32_t h[8];
+    for (int b = 0; b < 4; ++b) {
+        h[b] = mul_f16x2(lo[b], s2);
+        h[4 + b] = mul_f16x2(hi[b], s2);
+    }
+    const uint32_t base = (g < 4) ? half0 : half1;
+    const int c = (g % 4) * 2;
+    st_shared_v4(base + sw128(row, c), h[0], h[1], h[2], h[3]);
+    st_shared_v4(base + sw128(row, c + 1), h[4], h[5], h[6], h[7]);
+}
+
+// Dequantise one 128-value row: 64 packed bytes at `packed` (four 16-byte
+// chunks, two groups each) and 8 scale codes -> f16 in the swizzled layout.
+// The chunks are read starting at chunk `rot`, so that the rows a warp reads
+// together (64 bytes apart) fall in distinct banks when rot = (row / 2) % 4.
+__device__ __forceinline__ void dequant_row(const uint4* packed, uint2 scales, uint32_t half0,
+                                            uint32_t half1, int row, int rot)
+{
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            h[b] = mul_f16x2(e2m1x2_to_f16x2((w0 >> (8 * b)) & 0xFF), s2);
-            h[4 + b] = mul_f16x2(e2m1x2_to_f16x2((w1 >> (8 * b)) & 0xFF), s2);
-        }
-        const uint32_t base = (g < 4) ? half0 : half1;
-        const int c = (g % 4) * 2;                // two 16-byte chunks per group
-        st_shared_v4(base + sw128(row, c), h[0], h[1], h[2], h[3]);
-        st_shared_v4(base + sw128(row, c + 1), h[4], h[5], h[6], h[7]);
+    for (int k = 0; k < 4; ++k) {
+        const int c = (k + rot) & 3;
+        const uint4 v = packed[c];
+        const uint32_t sw = c < 2 ? scales.x : scales.y;
+        dequant_group(v.x, v.y, (sw >> (16 * (c & 1))) & 0xFF, 2 * c, half0, half1, row);
+        dequant_group(v.z, v.w, (sw >> (16 * (c & 1) + 8)) & 0xFF, 2 * c + 1, half0, half1, row);
     }
 }
 
@@ -111,9 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int S = a.stages;
+    const int S = a.stages;     // staging slots
+    const int T = a.tiles;      // f16 tiles
     const int G = a.group_size;
-    const Nvfp4Layout L = nvfp4_layout(S);
+    const Nvfp4Layout L = nvfp4_layout(S, T);
 
     const uint32_t base = smem_addr(smem);
     const uint32_t tile_base = base + L.tile;
@@ -121,20 +140,22 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     const uint32_t scale_base = base + L.scales;
     const uint32_t q_base = base + L.q;
     const uint32_t bar = base + L.bar;
-    auto full_bar = [&](int s) { return bar + 8u * s; };
-    auto deq_bar = [&](int s) { return bar + 8u * (S + s); };
-    auto empty_bar = [&](int s) { return bar + 8u * (2 * S + s); };
-    const uint32_t tfull_bar0 = bar + 8u * (3 * S);
-    const uint32_t tempty_bar0 = bar + 8u * (3 * S + 2);
-    const uint32_t qfull_bar0 = bar + 8u * (3 * S + 4);
-    const uint32_t qempty_bar0 = bar + 8u * (3 * S + 6);
+    auto full_bar = [&](int s) { return bar + 8u * s; };                  // staging landed
+    auto sfree_bar = [&](int s) { return bar + 8u * (S + s); };           // staging read
+    auto deq_bar = [&](int t) { return bar + 8u * (2 * S + t); };         // tile written
+    auto tfree_bar = [&](int t) { return bar + 8u * (2 * S + T + t); };   // tile consumed
+    const uint32_t tfull_bar0 = bar + 8u * (2 * S + 2 * T);              // + 8*acc
+    const uint32_t tempty_bar0 = tfull_bar0 + 8u * 8;
+    const uint32_t qfull_bar0 = tempty_bar0 + 8u * 8;                    // + 8*slot
+    const uint32_t qempty_bar0 = qfull_bar0 + 8u * 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
     int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t kTmemCols = 32;    // two accumulators of N = 16 columns
+    constexpr int kAcc = 8;               // accumulators of N = 16 columns in flight
+    constexpr uint32_t kTmemCols = kAcc * kN;
 
     if (warp == kProducerWarp) {
         const long long total = warp_total_blocks(a.context_lengths, a.groups);
@@ -147,12 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             *abort_flag = 0;
             for (int s = 0; s < S; ++s) {
                 mbar_init(full_bar(s), 1 + 32);   // expect_tx arrive + each lane's cp.async
-                mbar_init(deq_bar(s), 4);
-                mbar_init(empty_bar(s), 4);
+                mbar_init(sfree_bar(s), 4);
             }
-            for (int i = 0; i < 2; ++i) {
+            for (int t = 0; t < T; ++t) {
+                mbar_init(deq_bar(t), 4);
+                mbar_init(tfree_bar(t), 1);       // the MMA's commit
+            }
+            for (int i = 0; i < kAcc; ++i) {
                 mbar_init(tfull_bar0 + 8u * i, 1);
                 mbar_init(tempty_bar0 + 8u * i, 4);
+            }
+            for (int i = 0; i < 2; ++i) {
                 mbar_init(qfull_bar0 + 8u * i, 4);
                 mbar_init(qempty_bar0 + 8u * i, 4);
             }
@@ -175,6 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
         int it = 0, prev_g = -1;
         long long bt_row = 0;
+        // block-table entries come 32 at a time, one per lane, the next 32
+        // already in flight: lane i of `cur` holds block cur_j + i
+        int nbl = 0, cur_j = 0, cur = 0, nxt = 0;
+        auto fetch = [&](int j0) {
+            return j0 + lane < nbl ? __ldg(a.block_table + bt_row + j0 + lane) : 0;
+        };
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
@@ -185,17 +217,27 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     req = 0;
                 }
                 bt_row = (long long)req * a.bt_stride;
+                nbl = blocks_of(min(w.len, a.max_context));
+                cur_j = w.j;
+                cur = fetch(cur_j);
+                nxt = fetch(cur_j + 32);
                 prev_g = w.b;
             }
             const int s = it % S;
-            if (lane == 0) ok = mbar_wait(empty_bar(s), ((it / S) & 1) ^ 1, abort_flag, a.status);
+            if (lane == 0) ok = mbar_wait(sfree_bar(s), ((it / S) & 1) ^ 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             long long page[2] = {0, 0};
             int nload = 0;
             for (int cc = 0; cc < c; ++cc) {
+                if (w.j + cc >= cur_j + 32) {
+                    cur_j += 32;
+                    cur = nxt;
+                    nxt = fetch(cur_j + 32);
+                }
+                const int entry = __shfl_sync(0xffffffffu, cur, (w.j + cc - cur_j) & 31);
                 if ((long long)(w.j + cc) * kBlockKeys < a.max_context) {
-                    long long pg = __ldg(a.block_table + bt_row + w.j + cc);
+                    long long pg = entry;
                     if (pg < 0 || pg >= a.num_pages) {
                         if (lane == 0) atomicOr(a.status, kStatusBadBlock);
                         pg = 0;
@@ -242,30 +284,31 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 ++qcount;
                 prev_g = w.b;
             }
-            const int s = it % S;
-            ok = mbar_wait(deq_bar(s), (it / S) & 1, abort_flag, a.status);
+            const int tt = it % T;
+            ok = mbar_wait(deq_bar(tt), (it / T) & 1, abort_flag, a.status);
             if (!ok) break;
-            const int acc = it & 1;
-            ok = mbar_wait(tempty_bar0 + 8u * acc, ((it >> 1) & 1) ^ 1, abort_flag, a.status);
+            const int acc = it % kAcc;
+            ok = mbar_wait(tempty_bar0 + 8u * acc, ((it / kAcc) & 1) ^ 1, abort_flag, a.status);
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t d = tmem_base + (uint32_t)(acc * kN);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint64_t ad = smem_desc_sw128(tile_base + s * kTileBytes + h * kHalfBytes);
+                    const uint64_t ad = smem_desc_sw128(tile_base + tt * kTileBytes + h * kHalfBytes);
                     const uint64_t bd = smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (h | k) ? 1u : 0u);
                 }
                 mma_commit(tfull_bar0 + 8u * acc);
+                mma_commit(tfree_bar(tt));        // the tile may be rewritten once these complete
             }
             __syncwarp();
             w.advance(c);
             ++it;
         }
-        if (!ok && it > 0) mbar_wait_drain(tfull_bar0 + 8u * ((it - 1) & 1), ((it - 1) >> 1) & 1);
+        if (!ok && it > 0) mbar_wait_drain(tfull_bar0 + 8u * ((it - 1) % kAcc), ((it - 1) / kAcc) & 1);
     } else if (warp >= kFirstEpiWarp && warp < kFirstDeqWarp) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
@@ -286,9 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 len = min(__ldg(a.context_lengths + w.b), a.max_context);
             }
             const bool last = w.last_of_request(c);
-            const int s = it % S;
-            const int acc = it & 1;
-            ok = mbar_wait(tfull_bar0 + 8u * acc, (it >> 1) & 1, abort_flag, a.status);
+            const int acc = it % kAcc;
+            ok = mbar_wait(tfull_bar0 + 8u * acc, (it / kAcc) & 1, abort_flag, a.status);
             if (!ok) break;
             tc_fence_after();
             float v[8];
@@ -304,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(tempty_bar0 + 8u * acc);
-                mbar_arrive(empty_bar(s));
                 if (last) mbar_arrive(qempty_bar0 + 8u * slot);
             }
             w.advance(c);
@@ -332,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
                     const uint2 sc =
                         __ldg(reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
-                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t);
+                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
                 } else if (t < kN) {
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -346,22 +387,27 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 ++qcount;
                 prev_g = w.b;
             }
-            const int s = it % S;
+            const int s = it % S, tt = it % T;
             ok = mbar_wait(full_bar(s), (it / S) & 1, abort_flag, a.status);
             if (!ok) break;
             const int pg = t >> 6, r = t & 63;
-            if (pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context) {
+            const bool mine = pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context;
+            ok = mbar_wait(tfree_bar(tt), ((it / T) & 1) ^ 1, abort_flag, a.status);
+            if (!ok) break;
+            if (mine) {
                 const uint4* src = reinterpret_cast<const uint4*>(
                     smem + L.packed + (2 * s + pg) * kPackedPage + r * kPackedRow);
-                const uint4 pk[4] = {src[0], src[1], src[2], src[3]};
                 const uint2 sc = *reinterpret_cast<const uint2*>(
                     smem + L.scales + (2 * s + pg) * kScalePage + r * kScalesPerRow);
-                const uint32_t h0 = tile_base + s * kTileBytes + pg * kPageHalfBytes;
-                dequant_row(pk, sc, h0, h0 + kHalfBytes, r);
+                const uint32_t h0 = tile_base + tt * kTileBytes + pg * kPageHalfBytes;
+                dequant_row(src, sc, h0, h0 + kHalfBytes, r, (r >> 1) & 3);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(deq_bar(s));
+            if (lane == 0) {
+                mbar_arrive(sfree_bar(s));        // staging slot read: refill it
+                mbar_arrive(deq_bar(tt));
+            }
             w.advance(c);
             ++it;
         }
@@ -377,11 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
 
 }  // namespace
 
-size_t nvfp4_smem_bytes(int stages) { return (size_t)nvfp4_layout(stages).total + 1024; }
+size_t nvfp4_smem_bytes(int stages, int tiles)
+{
+    return (size_t)nvfp4_layout(stages, tiles).total + 1024;
+}
 
 cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream)
 {
-    const size_t smem = nvfp4_smem_bytes(a.stages);
+    const size_t smem = nvfp4_smem_bytes(a.stages, a.tiles);
     static int configured_device = -1;
     static size_t configured_smem = 0;
     int dev = 0;

@@ -484,6 +484,20 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte)
     return h;
 }
 
+// The four bytes of w (eight E2M1 codes, low nibble first) to four f16x2,
+// byte i -> h[i], exactly.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
 // An E4M3 code to an f16x2 holding its value twice, exactly.
 __device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code)
 {
