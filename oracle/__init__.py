@@ -274,3 +274,41 @@ def fp8_written_mask(seq_lens, next_n: int, max_context: int) -> np.ndarray:
     requests)."""
     sl = np.repeat(np.asarray(seq_lens, dtype=np.int64), next_n)
     return np.arange(max_context)[None, :] < sl[:, None]
+
+
+def _order_key(values: np.ndarray) -> np.ndarray:
+    """Unsigned keys whose order is the order of the float32 values they come
+    from (negative values have their bits inverted, the rest their sign bit
+    set): -NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN."""
+    bits = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32)
+    neg = (bits >> np.uint32(31)).astype(bool)
+    return np.where(neg, ~bits, bits | np.uint32(0x80000000)).astype(np.uint32)
+
+
+def topk_logits(logits, seq_lens, next_n: int, max_context: int, k: int):
+    """The indexer's selection over paged MQA logits ("flashinfer.attn_scores",
+    intro: the logits are what a sparse-attention indexer uses to choose which
+    KV tokens to keep; the note: row b*next_n+t is meaningful for positions
+    0 .. seq_lens[b]-next_n+t).  For each row, the k positions with the
+    largest logits among p <= min(seq_lens[b]-next_n+t, max_context-1), in
+    descending order of value (float32 bit order, see ``_order_key``), equal
+    values in ascending position; fewer candidates than k leave the remaining
+    slots as index -1 and value -inf.  Rows of empty requests have no
+    candidates.  Returns ``(indices int32 [rows, k], values float32 [rows, k])``.
+    """
+    x = np.asarray(logits, dtype=np.float32)
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    rows = sl.shape[0] * next_n
+    idx = np.full((rows, k), -1, dtype=np.int32)
+    val = np.full((rows, k), -np.inf, dtype=np.float32)
+    for r in range(rows):
+        b, t = divmod(r, next_n)
+        lim = min(int(sl[b]) - next_n + t + 1, max_context) if sl[b] > 0 else 0
+        if lim <= 0:
+            continue
+        keys = _order_key(x[r, :lim]).astype(np.int64)
+        pos = np.arange(lim)
+        order = np.lexsort((pos, -keys))[:k]         # key descending, then position
+        idx[r, :order.shape[0]] = order
+        val[r, :order.shape[0]] = x[r, order]
+    return idx, val
