@@ -218,6 +218,31 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
                              int64_t scores_stride, int max_context, void* stream);
 
 /*
+ * pml_topk_logits -- the indexer's selection over the logits
+ * ("flashinfer.attn_scores", intro: the logits are what a sparse-attention
+ * indexer uses to choose which KV tokens to keep; note: row b*next_n+t is
+ * meaningful for positions 0 .. seq_lens[b]-next_n+t).  The pages fix neither
+ * k nor the order of equal values; this call's definition:
+ *
+ *   indices[r, 0..k) = the k positions p < min(seq_lens[b]-next_n+t+1,
+ *   max_context) with the largest logits[r, p], r = b*next_n+t, in descending
+ *   order of value -- the float32 bit order, -NaN < -inf < ... < -0 < +0 < ...
+ *   < +inf < +NaN -- equal values in ascending position; slots past the
+ *   number of candidates hold -1 (values: -inf).  Requests with
+ *   seq_lens[b] <= 0 have no candidates.
+ *
+ * logits    fp32 [batch*next_n, logits_stride], logits_stride >= max_context
+ *           (only candidate positions are read)
+ * indices   int32 [batch*next_n, indices_stride], indices_stride >= k (written)
+ * values    NULL, or fp32 [batch*next_n, values_stride] (written: the
+ *           selected logits, bit for bit)
+ * k         1 .. 4096 (else PML_ERR_UNSUPPORTED); next_n >= 1
+ */
+int pml_topk_logits(const float* logits, int64_t logits_stride, const int32_t* seq_lens, int batch,
+                    int next_n, int max_context, int k, int32_t* indices, int64_t indices_stride,
+                    float* values, int64_t values_stride, void* stream);
+
+/*
  * pml_fp8_paged_mqa_logits_noalloc -- the two-step call (pml_schedule, then
  * pml_fp8_paged_mqa_logits with that schedule) for callers that cannot
  * allocate device memory.  The documentation pages have no counterpart: it

@@ -17,6 +17,8 @@ Entry points (same names as the C ABI):
 * ``pml_indexer_scores_bf16`` -- the single-head bf16 case
   ("flashinfer.sdsa.indexer_scores").
 * ``pml_indexer_scores_nvfp4`` -- the same over NVFP4 queries and keys.
+* ``pml_topk_logits`` -- the indexer's selection: each row's k largest
+  logits among its meaningful positions.
 
 ``fp8_paged_mqa_logits`` / ``indexer_scores`` wrap them with the pages'
 keyword style (``out=``, ``schedule_meta=``, ``scores=``).
@@ -31,7 +33,8 @@ import torch
 __all__ = [
     "PmlError", "lib", "library_path", "pml_schedule", "pml_fp8_paged_mqa_logits",
     "pml_fp8_paged_mqa_logits_ex",
-    "pml_indexer_scores_bf16", "pml_indexer_scores_nvfp4", "pml_fp8_paged_mqa_logits_noalloc",
+    "pml_indexer_scores_bf16", "pml_indexer_scores_nvfp4", "pml_topk_logits",
+    "pml_fp8_paged_mqa_logits_noalloc",
     "pml_device_status",
     "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
     "fp8_paged_mqa_logits", "indexer_scores", "compute_paged_mqa_logits_schedule",
@@ -89,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.pml_indexer_scores_nvfp4.argtypes = [P, P, i32, P, i64, P, i64, i64, P, i64, i32, P, P,
                                                i32, P, i64, i32, P]
         L.pml_indexer_scores_nvfp4.restype = i32
+        L.pml_topk_logits.argtypes = [P, i64, P, i32, i32, i32, i32, P, i64, P, i64, P]
+        L.pml_topk_logits.restype = i32
         L.pml_fp8_paged_mqa_logits_noalloc.argtypes = [P, P, i64, P, P, P, i64, i32, P, i64, i32,
                                                        i32, i32, i32, P]
         L.pml_fp8_paged_mqa_logits_noalloc.restype = i32
@@ -267,6 +272,32 @@ def pml_indexer_scores_bf16(query: torch.Tensor, key_cache: torch.Tensor, page_s
         _ptr(requests), context_lengths.numel(), _ptr(scores), scores.stride(0), max_context,
         _stream(stream)), "pml_indexer_scores_bf16")
     return scores
+
+
+def pml_topk_logits(logits: torch.Tensor, seq_lens: torch.Tensor, next_n: int, max_context: int,
+                    k: int, indices: torch.Tensor | None = None,
+                    values: torch.Tensor | None = None, stream=None):
+    """Each row's ``k`` largest logits among positions ``p <= seq_lens[b] -
+    next_n + t`` (and ``< max_context``), descending, equal values by
+    position; -1 / -inf past the candidates.  Returns ``(indices, values)``;
+    ``values`` only if given."""
+    _cuda(logits, "logits", contiguous=False)
+    _cuda(seq_lens, "seq_lens")
+    if logits.dtype != torch.float32 or logits.stride(-1) != 1:
+        raise ValueError("logits must be float32 with unit last stride")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    rows = seq_lens.numel() * next_n
+    if indices is None:
+        indices = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    _cuda(indices, "indices", contiguous=False)
+    if values is not None:
+        _cuda(values, "values", contiguous=False)
+    _check(lib().pml_topk_logits(
+        _ptr(logits), logits.stride(0), _ptr(seq_lens), seq_lens.numel(), next_n, max_context, k,
+        _ptr(indices), indices.stride(0), _ptr(values), values.stride(0) if values is not None else 0,
+        _stream(stream)), "pml_topk_logits")
+    return indices, values
 
 
 def pml_indexer_scores_nvfp4(query: torch.Tensor, query_scales: torch.Tensor,

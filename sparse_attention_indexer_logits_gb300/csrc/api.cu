@@ -241,6 +241,36 @@ int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 
+int pml_topk_logits(const float* logits, int64_t logits_stride, const int32_t* seq_lens, int batch,
+                    int next_n, int max_context, int k, int32_t* indices, int64_t indices_stride,
+                    float* values, int64_t values_stride, void* stream)
+{
+    if (batch < 0 || next_n < 1 || max_context < 1) return PML_ERR_INVALID_ARG;
+    if (k < 1 || k > kTopkMax) return PML_ERR_UNSUPPORTED;
+    if (batch == 0) return PML_OK;
+    if (!logits || !seq_lens || !indices) return PML_ERR_INVALID_ARG;
+    const long long rows = (long long)batch * next_n;
+    if (rows > 0x7fffffffLL) return PML_ERR_INVALID_ARG;
+    if (logits_stride < max_context || indices_stride < k) return PML_ERR_INVALID_ARG;
+    if (values && values_stride < k) return PML_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(seq_lens, 4) || !aligned(indices, 4) ||
+        !aligned(values, 4))
+        return PML_ERR_ALIGNMENT;
+    TopkArgs a;
+    a.logits = logits;
+    a.seq_lens = seq_lens;
+    a.indices = indices;
+    a.values = values;
+    a.logits_stride = logits_stride;
+    a.indices_stride = indices_stride;
+    a.values_stride = values_stride;
+    a.next_n = next_n;
+    a.max_context = max_context;
+    a.k = k;
+    const cudaError_t e = launch_topk(a, (int)rows, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PML_OK : cuda_fail(e);
+}
+
 int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, int rows,
                              const uint8_t* key_cache, int64_t page_stride_bytes,
                              const uint8_t* key_scales, int64_t scale_page_stride_bytes,

@@ -67,6 +67,21 @@ struct Nvfp4Args {
     int tiles;       // f16 tiles the MMA reads
 };
 
+constexpr int kTopkMax = 4096;     // largest k of the top-k selection
+
+struct TopkArgs {
+    const float* logits;
+    const int32_t* seq_lens;
+    int32_t* indices;
+    float* values;                // may be null
+    long long logits_stride;
+    long long indices_stride;
+    long long values_stride;
+    int next_n;
+    int max_context;
+    int k;
+};
+
 // Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
 size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
@@ -77,6 +92,7 @@ cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUte
 cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
                                const Bf16Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_topk(const TopkArgs& a, int rows, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
                             cudaStream_t stream);
 

@@ -451,3 +451,30 @@ def indexer_nvfp4(group_size: int, seed: int = 6, groups: int = 256, max_context
     req[lens == 0] = np.int32(-123456789)     # a group of length 0 may name any request
     p.requests = req
     return p
+
+
+# ---------------------------------------------------------------- top-k input
+
+def topk_logits_input(batch: int, next_n: int, max_context: int, seed: int = 9,
+                      lo: int = 0, hi: int | None = None, distinct: int | None = None,
+                      specials: bool = True):
+    """Synthetic logits rows [batch*next_n, max_context] and seq_lens for the
+    top-k selection: values ~N(0, 4) (or ``distinct`` levels only, for many
+    ties), seq_lens uniform on [lo, hi] (default [0, max_context]); with
+    ``specials`` some rows carry +-inf, signed zeros and a NaN."""
+    g = rng(seed)
+    hi = max_context if hi is None else hi
+    seq_lens = g.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
+    rows = batch * next_n
+    if distinct:
+        x = g.integers(-distinct // 2, distinct - distinct // 2, size=(rows, max_context))
+        x = x.astype(np.float32)
+    else:
+        x = (g.standard_normal((rows, max_context), dtype=np.float32) * 4).astype(np.float32)
+    if specials and rows > 0 and max_context >= 8:
+        r = g.integers(0, rows, size=4)
+        x[r[0], :4] = [np.inf, -np.inf, -0.0, 0.0]
+        x[r[1], 1] = np.nan
+        x[r[2], 2] = -np.nan
+        x[r[3], 3] = np.float32(3.4e38)
+    return x, seq_lens

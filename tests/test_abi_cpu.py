@@ -142,6 +142,20 @@ def test_nvfp4_argument_checks(L):
     assert _nvfp4(L, sc_stride=100) == 1 and _nvfp4(L, bt_stride=2) == 1
 
 
+def test_topk_argument_checks(L):
+    def topk(**o):
+        a = dict(x=P, xs=256, sl=P, batch=2, n=1, mc=256, k=16, idx=P, ids=16, val=None, vs=0)
+        a.update(o)
+        return L.pml_topk_logits(a["x"], a["xs"], a["sl"], a["batch"], a["n"], a["mc"], a["k"],
+                                 a["idx"], a["ids"], a["val"], a["vs"], None)
+    assert topk(batch=0) == 0
+    assert topk(k=0) == 2 and topk(k=4097) == 2
+    assert topk(x=None) == 1 and topk(idx=None) == 1
+    assert topk(xs=100) == 1 and topk(ids=8) == 1
+    assert topk(val=P, vs=8) == 1
+    assert topk(x=P + 2) == 3 and topk(idx=P + 1) == 3
+
+
 def test_schedule_argument_checks(L):
     assert L.pml_schedule(P, 4, 1, 0, P, None) == 1
     assert L.pml_schedule(P, 4, 1, 8, None, None) == 1
