@@ -267,7 +267,10 @@ int pml_topk_logits(const float* logits, int64_t logits_stride, const int32_t* s
     a.next_n = next_n;
     a.max_context = max_context;
     a.k = k;
-    const cudaError_t e = launch_topk(a, (int)rows, static_cast<cudaStream_t>(stream));
+    DeviceInfo dev;
+    cudaError_t e = device_info(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_topk(a, (int)rows, dev.smem_optin, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 

@@ -92,7 +92,7 @@ cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUte
 cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
                                const Bf16Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream);
-cudaError_t launch_topk(const TopkArgs& a, int rows, cudaStream_t stream);
+cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
                             cudaStream_t stream);
 

@@ -13,7 +13,9 @@
 // exact key T of the K-th largest candidate (K = min(k, lim)); one more pass
 // collects every key above T, and the first (in position order) of the keys
 // equal to T through a block-wide scan; a bitonic sort of (key, ~position)
-// pairs in shared memory gives the output order.
+// pairs in shared memory gives the output order.  A row whose candidates fit
+// in the rest of shared memory is read from global memory once and the five
+// passes run on that copy.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -24,7 +26,7 @@ namespace pml {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
 // Keys and values stay integer bit patterns throughout: a float register can
@@ -46,12 +48,25 @@ __device__ __forceinline__ unsigned long long pack_cand(uint32_t key, int p)
     return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)p);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
+// The candidates' bit patterns: from the shared-memory copy of the row when
+// it fits (`cached`), else from global memory.
+struct RowSource {
+    const uint32_t* gx;
+    const uint32_t* sx;
+    bool cached;
+    __device__ __forceinline__ uint32_t operator()(int p) const
+    {
+        return cached ? sx[p] : __ldg(gx + p);
+    }
+};
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems)
 {
     __shared__ unsigned int hist[256];
     __shared__ unsigned long long cand[kTopkMax];
     __shared__ int warp_sums[kWarps];
     __shared__ int sel[2];
+    extern __shared__ uint32_t row_cache[];
 
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
@@ -61,7 +76,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
     int lim = len > 0 ? min(len - a.next_n + t + 1, a.max_context) : 0;
     if (lim < 0) lim = 0;
     const int K = min(a.k, lim);
-    const uint32_t* x = reinterpret_cast<const uint32_t*>(a.logits) + (long long)row * a.logits_stride;
+    const uint32_t* gx =
+        reinterpret_cast<const uint32_t*>(a.logits) + (long long)row * a.logits_stride;
+    // one read of the row from global memory when it fits in shared memory
+    const bool cached = lim <= cache_elems;
+    if (cached) {
+        for (int p = tid; p < lim; p += kThreads) row_cache[p] = __ldg(gx + p);
+        __syncthreads();
+    }
+    const RowSource x{gx, row_cache, cached};
 
     // radix select of the K-th largest key
     uint32_t prefix = 0, mask = 0;
@@ -70,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
         for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
         __syncthreads();
         for (int p = tid; p < lim; p += kThreads) {
-            const uint32_t key = order_key(__ldg(x + p));
+            const uint32_t key = order_key(x(p));
             if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
@@ -118,13 +141,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
         if (tid == 0) sel[0] = 0;
         __syncthreads();
         for (int p = tid; p < lim; p += kThreads) {
-            const uint32_t key = order_key(__ldg(x + p));
+            const uint32_t key = order_key(x(p));
             if (key > prefix) cand[atomicAdd(&sel[0], 1)] = pack_cand(key, p);
         }
         int taken = 0;
         for (int base = 0; base < lim && taken < need; base += kThreads) {
             const int p = base + tid;
-            const bool eq = p < lim && order_key(__ldg(x + p)) == prefix;
+            const bool eq = p < lim && order_key(x(p)) == prefix;
             const unsigned bal = __ballot_sync(0xffffffffu, eq);
             if (lane == 0) warp_sums[warp] = __popc(bal);
             __syncthreads();
@@ -181,9 +204,25 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs& a, int rows, cudaStream_t stream)
+cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream)
 {
-    topk_kernel<<<rows, kThreads, 0, stream>>>(a);
+    // static shared memory of the kernel, plus the largest row copy that fits
+    constexpr int kStatic = 256 * 4 + kTopkMax * 8 + kWarps * 4 + 8;
+    const int cache_bytes = (smem_optin - kStatic - 1024) & ~15;
+    const int cache_elems = cache_bytes > 0 ? cache_bytes / 4 : 0;
+    static int configured_device = -1;
+    static int configured_bytes = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev || configured_bytes != cache_bytes) {
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 cache_bytes > 0 ? cache_bytes : 0);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+        configured_bytes = cache_bytes;
+    }
+    topk_kernel<<<rows, kThreads, cache_bytes > 0 ? cache_bytes : 0, stream>>>(a, cache_elems);
     return cudaGetLastError();
 }
 
