@@ -42,6 +42,8 @@ WORKLOAD_TEXT = {
     "mtp4": "MTP verify: batch 32, next_n 4, 64 heads, seq_lens U[8192,65536], decode layout",
     "skewed": "skewed: 16 requests, next_n 1, 64 heads, one 131072, three empty, twelve "
               "U[512,4096]",
+    "topk_decode": "indexer top-k selection: 64 logits rows of 32768 (lengths U[1024,32768]), "
+                   "k 2048, indices of the largest meaningful logits",
     "nvfp4_g8": "single-head NVFP4 indexer_scores: 256 groups of 8 rows, E2M1 codes with E4M3 "
                 "scales per 16 values, pages of 4096 code bytes then 512 scale bytes, "
                 "context_lengths U[0,65536] (8 zeros), fp32 scores [2048, 65536]",
@@ -65,6 +67,8 @@ def make_problem(workload: str, rank: int):
         return W.mtp(next_n=n, seed=(2 if n == 4 else 3) + off, poison=False)
     if workload == "skewed":
         return W.skewed(seed=4 + off)
+    if workload == "topk_decode":
+        return W.topk_decode(seed=13 + off)
     if workload.startswith("nvfp4_g"):
         return W.indexer_nvfp4(group_size=int(workload[len("nvfp4_g"):]), seed=6 + off,
                                poison=False)
@@ -73,13 +77,24 @@ def make_problem(workload: str, rank: int):
     raise SystemExit(f"unknown workload {workload}")
 
 
-def kernel_fingerprint() -> str:
+# Sources each kernel is built from (the shared headers included): a recorded
+# traffic figure stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "fp8_logits_kernel": ("fp8_logits.cuh", "fp8_logits.cu", "fp8_logits_h8.cu", "fp8_logits_h16.cu",
+                          "fp8_logits_h32.cu", "fp8_logits_h64.cu"),
+    "bf16_scores_kernel": ("bf16_scores.cu",),
+    "nvfp4_scores_kernel": ("nvfp4_scores.cu",),
+    "topk_kernel": ("topk.cu",),
+}
+SHARED_SOURCES = ("common.cuh", "ptx.cuh", "kernels.h")
+
+
+def kernel_fingerprint(kernel: str) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sparse_attention_indexer_logits_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel] + SHARED_SOURCES):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -101,7 +116,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(path) as f:
         d = json.load(f)
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("fingerprint") != kernel_fingerprint():
+    if not e or e.get("fingerprint") != kernel_fingerprint(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -263,7 +278,10 @@ def config_of(workload, p, world, l2="rotate", copies=3):
     cfg = {"workload": WORKLOAD_TEXT.get(workload, workload),
            "l2": l2_text,
            "parallelism": "replicas" if world == 1 else f"dp{world} (independent batches)"}
-    if hasattr(p, "next_n"):
+    if hasattr(p, "k"):
+        cfg.update({"rows": int(p.logits.shape[0]), "k": p.k, "max_context": p.max_context,
+                    "positions_per_step": p.positions})
+    elif hasattr(p, "next_n"):
         cfg.update({"batch": p.batch, "next_n": p.next_n, "num_heads": p.num_heads,
                     "head_dim": 128, "positions_per_step": p.positions,
                     "max_context": p.max_context})
@@ -317,14 +335,26 @@ def main():
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     p = make_problem(args.workload, rank)
-    is_fp8 = hasattr(p, "next_n")
     from sparse_attention_indexer_logits_gb300 import workloads as W
+    is_topk = isinstance(p, W.TopkProblem)
+    is_fp8 = hasattr(p, "next_n")
     is_nvfp4 = isinstance(p, W.Nvfp4Problem)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     copies = args.copies if args.l2 == "rotate" else 1
     out_dtype = torch.bfloat16 if (is_fp8 and args.out_dtype == "bfloat16") else torch.float32
-    if is_fp8:
+    if is_topk:
+        def device_set():
+            return dict(x=t(p.logits), sl=t(p.seq_lens),
+                        out=torch.zeros((p.logits.shape[0], p.k), dtype=torch.int32, device=dev))
+        sets = [device_set() for _ in range(copies)]
+
+        def step(d, stream=None):
+            pml.pml_topk_logits(d["x"], d["sl"], p.rows_per_request, p.max_context, p.k,
+                                indices=d["out"], stream=stream)
+        kernel = "topk_kernel"
+        bound_name = "hbm"
+    elif is_fp8:
         def device_set():
             return dict(q=t(p.q), kv=t(p.kv_fused), w=t(p.weights), sl=t(p.seq_lens),
                         bt=t(p.block_table),
@@ -413,7 +443,20 @@ def main():
 
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
-    if is_fp8:
+    if is_topk:
+        d0 = sets[0]
+        inputs = ((d0["x"], torch.from_numpy(p.logits).pin_memory()),
+                  (d0["sl"], torch.from_numpy(p.seq_lens).pin_memory()))
+        hout = torch.empty(d0["out"].shape, dtype=torch.int32).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for _, h in inputs)
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d, h in inputs:
+                d.copy_(h, non_blocking=True)
+            step(d0)
+            hout.copy_(d0["out"], non_blocking=True)
+    elif is_fp8:
         hq, hkv, hw = (torch.from_numpy(a).pin_memory() for a in (p.q, p.kv_fused, p.weights))
         hsl, hbt = torch.from_numpy(p.seq_lens).pin_memory(), torch.from_numpy(p.block_table).pin_memory()
         d0 = sets[0]
@@ -475,7 +518,8 @@ def main():
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    alg_bytes = p.algorithmic_bytes(out_dtype.itemsize) if is_fp8 else p.algorithmic_bytes()
+    alg_bytes = (p.algorithmic_bytes(out_dtype.itemsize) if (is_fp8 and not is_topk)
+                 else p.algorithmic_bytes())
     achieved_gbs = alg_bytes / avg_launch_s / 1e9
     roof = {"bound": bound_name, "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved_gbs / hbm_peak, "traffic": recorded_traffic(kernel, args.workload),
@@ -491,7 +535,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": (("e4m3 x e4m3 -> f32" + (" -> bf16 out" if out_dtype == torch.bfloat16 else ""))
                       if is_fp8 else ("nvfp4 (e2m1 x e4m3/16) -> f16 x f16 -> f32" if is_nvfp4
-                                      else "bf16 x bf16 -> f32")),
+                                      else ("f32 logits -> int32 indices" if is_topk
+                                            else "bf16 x bf16 -> f32"))),
             "data": "synthetic (seeded generators; no public dataset on the pages)",
             "config": dict(config_of(args.workload, p, world, args.l2, copies),
                            **({"output_dtype": args.out_dtype} if is_fp8 else {})),

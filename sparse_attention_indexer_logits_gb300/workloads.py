@@ -478,3 +478,40 @@ def topk_logits_input(batch: int, next_n: int, max_context: int, seed: int = 9,
         x[r[2], 2] = -np.nan
         x[r[3], 3] = np.float32(3.4e38)
     return x, seq_lens
+
+
+@dataclass
+class TopkProblem:
+    """Synthetic logits rows for the top-k selection, shaped like a decode
+    step's output (batch rows of max_context positions)."""
+    name: str
+    logits: np.ndarray        # float32 [batch*rows_per_request, max_context]
+    seq_lens: np.ndarray      # int32 [batch]
+    rows_per_request: int     # next_n of the logits
+    max_context: int
+    k: int
+
+    @property
+    def candidates(self) -> np.ndarray:
+        n = self.rows_per_request
+        sl = np.repeat(self.seq_lens.astype(np.int64), n)
+        t = np.tile(np.arange(n), self.seq_lens.shape[0])
+        lim = np.where(sl > 0, np.minimum(sl - n + t + 1, self.max_context), 0)
+        return np.maximum(lim, 0)
+
+    @property
+    def positions(self) -> int:
+        return int(self.candidates.sum())
+
+    def algorithmic_bytes(self) -> int:
+        """Each candidate logit read once, k indices written per row."""
+        return int(self.candidates.sum() * 4 + self.logits.shape[0] * self.k * 4)
+
+    def algorithmic_flops(self) -> int:
+        return 0
+
+
+def topk_decode(seed: int = 13, k: int = 2048) -> TopkProblem:
+    """64 rows of 32768 logits with decode lengths U[1024, 32768], k = 2048."""
+    x, sl = topk_logits_input(64, 1, 32768, seed=seed, lo=1024, hi=32768, specials=False)
+    return TopkProblem("topk_decode", x, sl, 1, 32768, k)
