@@ -19,7 +19,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxFp8Stages = 12;
 constexpr int kMaxBf16Stages = 8;
 constexpr int kMaxNvfp4Stages = 16;
-constexpr int kNvfp4Tiles = 3;
+constexpr int kNvfp4Tiles = 4;   // even: two per side
 
 thread_local int g_last_cuda_error = 0;
 
@@ -324,14 +324,15 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
     a.groups = groups;
     a.group_size = G;
     a.max_context = max_context;
-    // a few f16 tiles (32 KB each) and as many staging slots (9 KB) as fit
+    // a few f16 tiles (32 KB each) and as many staging slots (9 KB) as fit;
+    // both split evenly between the kernel's two sides
     a.tiles = kNvfp4Tiles;
     const size_t fixed = nvfp4_smem_bytes(0, a.tiles);
     const size_t per_stage = nvfp4_smem_bytes(1, a.tiles) - fixed;
     if ((size_t)dev.smem_optin < fixed + 2 * per_stage) return PML_ERR_UNSUPPORTED;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
     if (stages > kMaxNvfp4Stages) stages = kMaxNvfp4Stages;
-    a.stages = stages;
+    a.stages = stages & ~1;
     e = launch_nvfp4_scores(a, dev.sm_count, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }

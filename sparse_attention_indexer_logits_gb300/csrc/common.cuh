@@ -114,6 +114,11 @@ struct Walk {
     {
         return (j + c == nbb) || (b == eb && j + c == ej);
     }
+    // blocks of request b in this range after the current tile
+    __device__ __forceinline__ int blocks_after(int c) const
+    {
+        return ((b == eb) ? ej : nbb) - j - c;
+    }
     __device__ __forceinline__ void advance(int c)
     {
         j += c;

@@ -16,23 +16,26 @@
 // operand with no rounding, and tcgen05.mma kind::f16 accumulates the exact
 // f16 products in fp32.
 //
-//   warp 0     producer: per tile one bulk copy per 4 KB page of packed keys
+//   (the producer, MMA and dequantising roles come twice, one copy for each
+//   side: the even tiles and the odd tiles)
+//   warps 0,10 producers: per tile one bulk copy per 4 KB page of packed keys
 //              and 8-byte cp.async copies of the 64 x 8 scale bytes (their
 //              pages need only 8-byte alignment), all completing on the
 //              staging slot's `full` barrier.  Staging slots (9 KB) are many
 //              and are freed as soon as the dequantising warps have read
 //              them; the f16 tiles (32 KB) are few and are freed by the MMA's
 //              commit, so most of the shared memory holds copies in flight.
-//   warp 1     MMA issue: 2 K-halves x 4 tcgen05.mma (K = 16) per tile
+//   warps 1,11 MMA issue: 2 K-halves x 4 tcgen05.mma (K = 16) per tile
 //              against the group's rows (padded to N = 16), one commit, into
-//              one of eight TMEM accumulators (16 columns each).
+//              one of eight TMEM accumulators (16 columns each; a side uses
+//              the four of its parity).
 //   warps 2-5  epilogue: one key per thread, up to 8 scores per key.
-//   warps 6-9  dequantisation: thread t expands key row t of the tile --
+//   warps 6-9, 12-15 dequantisation: thread t expands key row t of the tile --
 //              eight groups of 16 codes, cvt.rn.f16x2.e2m1x2 per byte pair
 //              and one f16x2 multiply by the group's scale -- into the
 //              128-byte-swizzled K-major layout the MMA reads (two K-halves
 //              of 64 values); per group of query rows, the same for the rows
-//              into one of two Q slots.
+//              into one of the side's two Q slots.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,15 +57,25 @@ constexpr int kTileBytes = 2 * kHalfBytes;               // 32 KB
 constexpr int kPageHalfBytes = kBlockKeys * 128;         // 8 KB
 constexpr int kQHalfBytes = kN * 128;                    // 2 KB
 constexpr int kQSlotBytes = 2 * kQHalfBytes;             // 4 KB
-constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kFirstEpiWarp = 2;
-constexpr int kFirstDeqWarp = 6;
-constexpr int kThreads = 320;
+// Two warps for each of the producer and MMA roles and two dequantising
+// warpgroups, each taking every other tile (side p = tile index & 1): one such
+// warp's per-tile chain (waits, lookups, copies or conversions) is longer than
+// a tile's share of HBM time.  Each side has its own half of the staging
+// slots, f16 tiles and Q slots, so every barrier has one side's roles on it,
+// in tile order.  One epilogue warpgroup takes every tile.
+constexpr int kProducerWarp = 0;      // and kProducerWarp2
+constexpr int kMmaWarp = 1;           // and kMmaWarp2; warp 1 also allocates TMEM
+constexpr int kFirstEpiWarp = 2;      // warps 2-5
+constexpr int kFirstDeqWarp = 6;      // warps 6-9, and 12-15
+constexpr int kProducerWarp2 = 10;
+constexpr int kMmaWarp2 = 11;
+constexpr int kFirstDeqWarp2 = 12;
+constexpr int kThreads = 512;
 
-// Two rings: `stages` staging slots of one tile's packed pages and scale bytes
-// (what HBM delivers; deep, so that many copies are in flight) and `tiles`
-// f16 tiles (what the MMA reads; short-lived: freed by the MMA's commit).
+// Two rings per side: `stages`/2 staging slots of one tile's packed pages and
+// scale bytes (what HBM delivers; deep, so that many copies are in flight) and
+// `tiles`/2 f16 tiles (what the MMA reads; short-lived: freed by the MMA's
+// commit); and two Q slots per side.
 struct Nvfp4Layout {
     uint32_t tile, packed, scales, q, bar, misc, total;
 };
@@ -74,8 +87,8 @@ __host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages, int tiles)
     L.packed = L.tile + (uint32_t)tiles * kTileBytes;
     L.scales = L.packed + (uint32_t)stages * 2 * kPackedPage;
     L.q = L.scales + (uint32_t)stages * 2 * kScalePage;
-    L.bar = L.q + 2 * kQSlotBytes;
-    L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 20) * 8;
+    L.bar = L.q + 4 * kQSlotBytes;
+    L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 24) * 8;
     L.total = L.misc + 64;
     return L;
 }
@@ -146,14 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     auto tfree_bar = [&](int t) { return bar + 8u * (2 * S + T + t); };   // tile consumed
     const uint32_t tfull_bar0 = bar + 8u * (2 * S + 2 * T);              // + 8*acc
     const uint32_t tempty_bar0 = tfull_bar0 + 8u * 8;
-    const uint32_t qfull_bar0 = tempty_bar0 + 8u * 8;                    // + 8*slot
-    const uint32_t qempty_bar0 = qfull_bar0 + 8u * 2;
+    const uint32_t qfull_bar0 = tempty_bar0 + 8u * 8;                    // + 8*(2*side+slot)
+    const uint32_t qempty_bar0 = qfull_bar0 + 8u * 4;
+    const int S2 = S / 2, T2 = T / 2;   // per side
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
     int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int prod = warp == kProducerWarp ? 0 : warp == kProducerWarp2 ? 1 : -1;
+    const int mmaw = warp == kMmaWarp ? 0 : warp == kMmaWarp2 ? 1 : -1;
+    const int dgrp = (warp >= kFirstDeqWarp && warp < kFirstDeqWarp + 4) ? 0
+                     : warp >= kFirstDeqWarp2 ? 1 : -1;
     constexpr int kAcc = 8;               // accumulators of N = 16 columns in flight
     constexpr uint32_t kTmemCols = kAcc * kN;
 
@@ -178,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 mbar_init(tfull_bar0 + 8u * i, 1);
                 mbar_init(tempty_bar0 + 8u * i, 4);
             }
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 mbar_init(qfull_bar0 + 8u * i, 4);
                 mbar_init(qempty_bar0 + 8u * i, 4);
             }
@@ -194,12 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     const uint32_t tmem_base = *tmem_slot;
     const int sb = sched[0], sj = sched[1], eb = sched[2], ej = sched[3];
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
+    if (prod >= 0) {
+        // ------------------------------------------------------------ producers
         const uint64_t policy = policy_evict_first();
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, prev_g = -1;
+        int it = 0, k = 0, prev_g = -1;   // it: tile; k: this side's tiles so far
         long long bt_row = 0;
         // block-table entries come 32 at a time, one per lane, the next 32
         // already in flight: lane i of `cur` holds block cur_j + i
@@ -210,6 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
+            if ((it & 1) != prod) {               // the other side's tile
+                w.advance(c);
+                ++it;
+                continue;
+            }
             if (w.b != prev_g) {
                 int req = __ldg(a.requests + w.b);
                 if (req < 0 || req >= a.num_requests) {
@@ -223,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 nxt = fetch(cur_j + 32);
                 prev_g = w.b;
             }
-            const int s = it % S;
-            if (lane == 0) ok = mbar_wait(sfree_bar(s), ((it / S) & 1) ^ 1, abort_flag, a.status);
+            const int s = prod * S2 + k % S2;
+            if (lane == 0) ok = mbar_wait(sfree_bar(s), ((k / S2) & 1) ^ 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             long long page[2] = {0, 0};
             int nload = 0;
             for (int cc = 0; cc < c; ++cc) {
-                if (w.j + cc >= cur_j + 32) {
+                while (w.j + cc >= cur_j + 32) {
                     cur_j += 32;
                     cur = nxt;
                     nxt = fetch(cur_j + 32);
@@ -262,54 +285,66 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             cp_async_arrive(full_bar(s));
             w.advance(c);
             ++it;
+            ++k;
         }
         if (!ok && lane == 0) {
-            for (int t = (it > S ? it - S : 0); t < it; ++t)
-                mbar_wait_drain(full_bar(t % S), (t / S) & 1);
+            for (int t = (k > S2 ? k - S2 : 0); t < k; ++t)
+                mbar_wait_drain(full_bar(prod * S2 + t % S2), (t / S2) & 1);
         }
         cp_async_wait_all();
-    } else if (warp == kMmaWarp) {
+    } else if (mmaw >= 0) {
         // ------------------------------------------------------------ MMA issue
         const uint32_t idesc = make_idesc(0, 0, kTileKeys, kN);   // f16 x f16 -> f32
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, qcount = 0, prev_g = -1, slot = 0;
+        // kg: tile within the request; qk: requests this side has tiles of
+        int it = 0, k = 0, kg = 0, prev_g = -1, qk = 0, slot = 0, last = -1;
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
             if (w.b != prev_g) {
-                slot = qcount & 1;
-                ok = mbar_wait(qfull_bar0 + 8u * slot, (qcount >> 1) & 1, abort_flag, a.status);
-                if (!ok) break;
-                ++qcount;
+                kg = 0;
                 prev_g = w.b;
             }
-            const int tt = it % T;
-            ok = mbar_wait(deq_bar(tt), (it / T) & 1, abort_flag, a.status);
-            if (!ok) break;
-            const int acc = it % kAcc;
-            ok = mbar_wait(tempty_bar0 + 8u * acc, ((it / kAcc) & 1) ^ 1, abort_flag, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t d = tmem_base + (uint32_t)(acc * kN);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t ad = smem_desc_sw128(tile_base + tt * kTileBytes + h * kHalfBytes);
-                    const uint64_t bd = smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (h | k) ? 1u : 0u);
+            if ((it & 1) == mmaw) {
+                if (kg < 2) {                     // this side's first tile of the request
+                    slot = 2 * mmaw + (qk & 1);
+                    ok = mbar_wait(qfull_bar0 + 8u * slot, (qk >> 1) & 1, abort_flag, a.status);
+                    if (!ok) break;
+                    ++qk;
                 }
-                mma_commit(tfull_bar0 + 8u * acc);
-                mma_commit(tfree_bar(tt));        // the tile may be rewritten once these complete
+                const int tt = mmaw * T2 + k % T2;
+                ok = mbar_wait(deq_bar(tt), (k / T2) & 1, abort_flag, a.status);
+                if (!ok) break;
+                const int acc = it % kAcc;        // this side's accumulators: it's parity
+                ok = mbar_wait(tempty_bar0 + 8u * acc, ((it / kAcc) & 1) ^ 1, abort_flag, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t d = tmem_base + (uint32_t)(acc * kN);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad =
+                            smem_desc_sw128(tile_base + tt * kTileBytes + h * kHalfBytes);
+                        const uint64_t bd =
+                            smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, (h | kk) ? 1u : 0u);
+                    }
+                    mma_commit(tfull_bar0 + 8u * acc);
+                    mma_commit(tfree_bar(tt));    // the tile may be rewritten once these complete
+                }
+                __syncwarp();
+                last = it;
+                ++k;
             }
-            __syncwarp();
             w.advance(c);
             ++it;
+            ++kg;
         }
-        if (!ok && it > 0) mbar_wait_drain(tfull_bar0 + 8u * ((it - 1) % kAcc), ((it - 1) / kAcc) & 1);
-    } else if (warp >= kFirstEpiWarp && warp < kFirstDeqWarp) {
+        if (!ok && last >= 0) mbar_wait_drain(tfull_bar0 + 8u * (last % kAcc), (last / kAcc) & 1);
+    } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
@@ -318,17 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, qcount = 0, prev_g = -1, slot = 0, len = 0;
+        int it = 0, prev_g = -1, len = 0, qk0 = 0, qk1 = 0;
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
             if (w.b != prev_g) {
-                slot = qcount & 1;
-                ++qcount;
                 prev_g = w.b;
                 len = min(__ldg(a.context_lengths + w.b), a.max_context);
             }
-            const bool last = w.last_of_request(c);
+            // the request's last two tiles are the last of each side: each
+            // frees its side's q slot
+            const bool last_of_side = w.blocks_after(c) <= 2;
+            const int side = it & 1;
             const int acc = it % kAcc;
             ok = mbar_wait(tfull_bar0 + 8u * acc, (it / kAcc) & 1, abort_flag, a.status);
             if (!ok) break;
@@ -346,70 +382,85 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(tempty_bar0 + 8u * acc);
-                if (last) mbar_arrive(qempty_bar0 + 8u * slot);
+                if (last_of_side)
+                    mbar_arrive(qempty_bar0 + 8u * (2 * side + ((side ? qk1 : qk0) & 1)));
+            }
+            if (last_of_side) {
+                if (side) ++qk1;
+                else ++qk0;
             }
             w.advance(c);
             ++it;
         }
-    } else {
+    } else if (dgrp >= 0) {
         // ------------------------------------------------------------ dequantisation
-        const int t = threadIdx.x - 32 * kFirstDeqWarp;   // key row of the tile, 0..127
+        const int t = threadIdx.x - 32 * (dgrp == 0 ? kFirstDeqWarp : kFirstDeqWarp2);   // row
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, qcount = 0, prev_g = -1;
+        int it = 0, k = 0, kg = 0, prev_g = -1, qk = 0;
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
             if (w.b != prev_g) {
-                // the group's query rows into the next Q slot (rows G..15 zero)
-                const int slot = qcount & 1;
-                ok = mbar_wait(qempty_bar0 + 8u * slot, ((qcount >> 1) & 1) ^ 1, abort_flag,
-                               a.status);
-                if (!ok) break;
-                const uint32_t qh0 = q_base + slot * kQSlotBytes;
-                if (t < G) {
-                    const long long qrow = (long long)w.b * G + t;
-                    const uint4* src = reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
-                    const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
-                    const uint2 sc =
-                        __ldg(reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
-                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
-                } else if (t < kN) {
+                kg = 0;
+                prev_g = w.b;
+            }
+            if ((it & 1) == dgrp) {
+                if (kg < 2) {
+                    // this side's first tile of the request: its query rows into
+                    // this side's next Q slot (rows G..15 zero)
+                    const int slot = 2 * dgrp + (qk & 1);
+                    ok = mbar_wait(qempty_bar0 + 8u * slot, ((qk >> 1) & 1) ^ 1, abort_flag,
+                                   a.status);
+                    if (!ok) break;
+                    const uint32_t qh0 = q_base + slot * kQSlotBytes;
+                    if (t < G) {
+                        const long long qrow = (long long)w.b * G + t;
+                        const uint4* src =
+                            reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
+                        const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2),
+                                             __ldg(src + 3)};
+                        const uint2 sc = __ldg(
+                            reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
+                        dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
+                    } else if (t < kN) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        st_shared_v4(qh0 + sw128(t, ch), 0u, 0u, 0u, 0u);
-                        st_shared_v4(qh0 + kQHalfBytes + sw128(t, ch), 0u, 0u, 0u, 0u);
+                        for (int ch = 0; ch < 8; ++ch) {
+                            st_shared_v4(qh0 + sw128(t, ch), 0u, 0u, 0u, 0u);
+                            st_shared_v4(qh0 + kQHalfBytes + sw128(t, ch), 0u, 0u, 0u, 0u);
+                        }
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
+                    ++qk;
+                }
+                const int s = dgrp * S2 + k % S2, tt = dgrp * T2 + k % T2;
+                ok = mbar_wait(full_bar(s), (k / S2) & 1, abort_flag, a.status);
+                if (!ok) break;
+                const int pg = t >> 6, r = t & 63;
+                const bool mine = pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context;
+                ok = mbar_wait(tfree_bar(tt), ((k / T2) & 1) ^ 1, abort_flag, a.status);
+                if (!ok) break;
+                if (mine) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        smem + L.packed + (2 * s + pg) * kPackedPage + r * kPackedRow);
+                    const uint2 sc = *reinterpret_cast<const uint2*>(
+                        smem + L.scales + (2 * s + pg) * kScalePage + r * kScalesPerRow);
+                    const uint32_t h0 = tile_base + tt * kTileBytes + pg * kPageHalfBytes;
+                    dequant_row(src, sc, h0, h0 + kHalfBytes, r, (r >> 1) & 3);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
-                ++qcount;
-                prev_g = w.b;
-            }
-            const int s = it % S, tt = it % T;
-            ok = mbar_wait(full_bar(s), (it / S) & 1, abort_flag, a.status);
-            if (!ok) break;
-            const int pg = t >> 6, r = t & 63;
-            const bool mine = pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context;
-            ok = mbar_wait(tfree_bar(tt), ((it / T) & 1) ^ 1, abort_flag, a.status);
-            if (!ok) break;
-            if (mine) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    smem + L.packed + (2 * s + pg) * kPackedPage + r * kPackedRow);
-                const uint2 sc = *reinterpret_cast<const uint2*>(
-                    smem + L.scales + (2 * s + pg) * kScalePage + r * kScalesPerRow);
-                const uint32_t h0 = tile_base + tt * kTileBytes + pg * kPageHalfBytes;
-                dequant_row(src, sc, h0, h0 + kHalfBytes, r, (r >> 1) & 3);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sfree_bar(s));        // staging slot read: refill it
-                mbar_arrive(deq_bar(tt));
+                if (lane == 0) {
+                    mbar_arrive(sfree_bar(s));    // staging slot read: refill it
+                    mbar_arrive(deq_bar(tt));
+                }
+                ++k;
             }
             w.advance(c);
             ++it;
+            ++kg;
         }
     }
 
