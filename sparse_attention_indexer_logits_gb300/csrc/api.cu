@@ -324,6 +324,10 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
     a.groups = groups;
     a.group_size = G;
     a.max_context = max_context;
+    a.fused = (key_scales == key_cache + (int64_t)kBlockKeys * kHeadDim / 2 &&
+               scale_page_stride_bytes == page_stride_bytes)
+                  ? 1
+                  : 0;
     // a few f16 tiles (32 KB each) and as many staging slots (9 KB) as fit;
     // both split evenly between the kernel's two sides
     a.tiles = kNvfp4Tiles;

@@ -65,6 +65,8 @@ struct Nvfp4Args {
     int max_context;
     int stages;      // staging slots (packed pages and scales of one tile)
     int tiles;       // f16 tiles the MMA reads
+    int fused;       // 1: a page's scales follow its codes (key_scales == key_cache + 4096,
+                     // one page stride), so one bulk copy brings both
 };
 
 constexpr int kTopkMax = 4096;     // largest k of the top-k selection

@@ -16,8 +16,8 @@
 // operand with no rounding, and tcgen05.mma kind::f16 accumulates the exact
 // f16 products in fp32.
 //
-//   (the producer, MMA and dequantising roles come twice, one copy for each
-//   side: the even tiles and the odd tiles)
+//   (every role comes twice, one copy for each side: the even tiles and the
+//   odd tiles)
 //   warps 0,10 producers: per tile one bulk copy per 4 KB page of packed keys
 //              and 8-byte cp.async copies of the 64 x 8 scale bytes (their
 //              pages need only 8-byte alignment), all completing on the
@@ -29,13 +29,13 @@
 //              against the group's rows (padded to N = 16), one commit, into
 //              one of eight TMEM accumulators (16 columns each; a side uses
 //              the four of its parity).
-//   warps 2-5  epilogue: one key per thread, up to 8 scores per key.
-//   warps 6-9, 12-15 dequantisation: thread t expands key row t of the tile --
-//              eight groups of 16 codes, cvt.rn.f16x2.e2m1x2 per byte pair
-//              and one f16x2 multiply by the group's scale -- into the
-//              128-byte-swizzled K-major layout the MMA reads (two K-halves
-//              of 64 values); per group of query rows, the same for the rows
-//              into one of the side's two Q slots.
+//   warps 2-5, 16-19 epilogues: one key per thread, up to 8 scores per key.
+//   warps 6-9, 12-15 dequantisation: thread t expands one 16-byte chunk
+//              (two groups of 16 codes) of four rows of the tile --
+//              cvt.rn.f16x2.e2m1x2 per byte and one f16x2 multiply by the
+//              group's scale -- into the 128-byte-swizzled K-major layout the
+//              MMA reads (two K-halves of 64 values); per group of query
+//              rows, whole rows into one of the side's two Q slots.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -52,41 +52,40 @@ constexpr int kPackedRow = kHeadDim / 2;                 // 64 bytes of codes pe
 constexpr int kScalesPerRow = kHeadDim / 16;             // 8
 constexpr int kPackedPage = kBlockKeys * kPackedRow;     // 4096
 constexpr int kScalePage = kBlockKeys * kScalesPerRow;   // 512
+constexpr int kStagePage = kPackedPage + kScalePage;     // 4608: a staged page, codes then scales
 constexpr int kHalfBytes = kTileKeys * 128;              // 16 KB: one f16 K-half of a tile
 constexpr int kTileBytes = 2 * kHalfBytes;               // 32 KB
-constexpr int kPageHalfBytes = kBlockKeys * 128;         // 8 KB
 constexpr int kQHalfBytes = kN * 128;                    // 2 KB
 constexpr int kQSlotBytes = 2 * kQHalfBytes;             // 4 KB
-// Two warps for each of the producer and MMA roles and two dequantising
-// warpgroups, each taking every other tile (side p = tile index & 1): one such
-// warp's per-tile chain (waits, lookups, copies or conversions) is longer than
-// a tile's share of HBM time.  Each side has its own half of the staging
-// slots, f16 tiles and Q slots, so every barrier has one side's roles on it,
-// in tile order.  One epilogue warpgroup takes every tile.
+// Every role comes twice, one copy for each side of the tile sequence (side
+// p = tile index & 1): one role's per-tile chain (waits, lookups, copy
+// issues, conversions, TMEM loads) is longer than a tile's share of HBM time.
+// Each side has its own half of the staging slots, f16 tiles, accumulators
+// and Q slots, so every barrier has one side's roles on it, in tile order.
 constexpr int kProducerWarp = 0;      // and kProducerWarp2
 constexpr int kMmaWarp = 1;           // and kMmaWarp2; warp 1 also allocates TMEM
-constexpr int kFirstEpiWarp = 2;      // warps 2-5
+constexpr int kFirstEpiWarp = 2;      // warps 2-5, and 16-19
 constexpr int kFirstDeqWarp = 6;      // warps 6-9, and 12-15
 constexpr int kProducerWarp2 = 10;
 constexpr int kMmaWarp2 = 11;
 constexpr int kFirstDeqWarp2 = 12;
-constexpr int kThreads = 512;
+constexpr int kFirstEpiWarp2 = 16;
+constexpr int kThreads = 640;
 
 // Two rings per side: `stages`/2 staging slots of one tile's packed pages and
 // scale bytes (what HBM delivers; deep, so that many copies are in flight) and
 // `tiles`/2 f16 tiles (what the MMA reads; short-lived: freed by the MMA's
 // commit); and two Q slots per side.
 struct Nvfp4Layout {
-    uint32_t tile, packed, scales, q, bar, misc, total;
+    uint32_t tile, stage, q, bar, misc, total;
 };
 
 __host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages, int tiles)
 {
     Nvfp4Layout L;
     L.tile = 0;
-    L.packed = L.tile + (uint32_t)tiles * kTileBytes;
-    L.scales = L.packed + (uint32_t)stages * 2 * kPackedPage;
-    L.q = L.scales + (uint32_t)stages * 2 * kScalePage;
+    L.stage = L.tile + (uint32_t)tiles * kTileBytes;             // slot s, page p: 2s + p
+    L.q = L.stage + (uint32_t)stages * 2 * kStagePage;
     L.bar = L.q + 4 * kQSlotBytes;
     L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 24) * 8;
     L.total = L.misc + 64;
@@ -137,6 +136,38 @@ __device__ __forceinline__ void dequant_row(const uint4* packed, uint2 scales, u
     }
 }
 
+// Position in a ring of n slots and the parity of its current pass, advanced
+// one step at a time (no division by the runtime ring size in the loops).
+struct RingPos {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n)
+    {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Dequantise one 16-byte chunk (32 codes: two groups of 16, scales sc & 0xFF
+// and sc >> 8) into four consecutive f16 chunks at dst + off[0..3].
+__device__ __forceinline__ void dequant_chunk(uint4 v, uint32_t sc, uint32_t dst,
+                                              const uint32_t (&off)[4])
+{
+    const uint32_t sa = e4m3_to_f16x2_dup(sc & 0xFF);
+    const uint32_t sb = e4m3_to_f16x2_dup(sc >> 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4];
+        e2m1x8_to_f16x2x4(w[q], h);
+        const uint32_t s2 = q < 2 ? sa : sb;
+        st_shared_v4(dst + off[q], mul_f16x2(h[0], s2), mul_f16x2(h[1], s2), mul_f16x2(h[2], s2),
+                     mul_f16x2(h[3], s2));
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Args a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -149,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
 
     const uint32_t base = smem_addr(smem);
     const uint32_t tile_base = base + L.tile;
-    const uint32_t packed_base = base + L.packed;
-    const uint32_t scale_base = base + L.scales;
+    const uint32_t stage_base = base + L.stage;
     const uint32_t q_base = base + L.q;
     const uint32_t bar = base + L.bar;
     auto full_bar = [&](int s) { return bar + 8u * s; };                  // staging landed
@@ -171,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     const int prod = warp == kProducerWarp ? 0 : warp == kProducerWarp2 ? 1 : -1;
     const int mmaw = warp == kMmaWarp ? 0 : warp == kMmaWarp2 ? 1 : -1;
     const int dgrp = (warp >= kFirstDeqWarp && warp < kFirstDeqWarp + 4) ? 0
-                     : warp >= kFirstDeqWarp2 ? 1 : -1;
+                     : (warp >= kFirstDeqWarp2 && warp < kFirstDeqWarp2 + 4) ? 1 : -1;
+    const int egrp = (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) ? 0
+                     : warp >= kFirstEpiWarp2 ? 1 : -1;
     constexpr int kAcc = 8;               // accumulators of N = 16 columns in flight
     constexpr uint32_t kTmemCols = kAcc * kN;
 
@@ -185,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
             *abort_flag = 0;
             for (int s = 0; s < S; ++s) {
-                mbar_init(full_bar(s), 1 + 32);   // expect_tx arrive + each lane's cp.async
+                // expect_tx arrive (+ each lane's cp.async of scales, unless fused)
+                mbar_init(full_bar(s), a.fused ? 1 : 1 + 32);
                 mbar_init(sfree_bar(s), 4);
             }
             for (int t = 0; t < T; ++t) {
@@ -218,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
         int it = 0, k = 0, prev_g = -1;   // it: tile; k: this side's tiles so far
+        RingPos sp;                        // this side's staging slot
         long long bt_row = 0;
         // block-table entries come 32 at a time, one per lane, the next 32
         // already in flight: lane i of `cur` holds block cur_j + i
@@ -246,46 +280,70 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 nxt = fetch(cur_j + 32);
                 prev_g = w.b;
             }
-            const int s = prod * S2 + k % S2;
-            if (lane == 0) ok = mbar_wait(sfree_bar(s), ((k / S2) & 1) ^ 1, abort_flag, a.status);
+            // the entries of blocks w.j and w.j + 1: `cur` and `nxt` hold the
+            // window [cur_j, cur_j + 64), which covers both
+            while (w.j >= cur_j + 32) {
+                cur_j += 32;
+                cur = nxt;
+                nxt = fetch(cur_j + 32);
+            }
+            const int i0 = w.j - cur_j;
+            const int e0 = __shfl_sync(0xffffffffu, cur, i0);
+            const int e1c = __shfl_sync(0xffffffffu, cur, (i0 + 1) & 31);
+            const int e1n = __shfl_sync(0xffffffffu, nxt, 0);
+            // pages of the tile below max_context
+            const int nload = (long long)w.j * kBlockKeys >= a.max_context ? 0
+                              : (c > 1 && (long long)(w.j + 1) * kBlockKeys < a.max_context) ? 2
+                                                                                             : 1;
+            long long page0 = e0, page1 = i0 < 31 ? e1c : e1n;
+            if (nload >= 1 && (page0 < 0 || page0 >= a.num_pages)) {
+                if (lane == 0) atomicOr(a.status, kStatusBadBlock);
+                page0 = 0;
+            }
+            if (nload == 2 && (page1 < 0 || page1 >= a.num_pages)) {
+                if (lane == 0) atomicOr(a.status, kStatusBadBlock);
+                page1 = 0;
+            }
+            const int s = prod * S2 + sp.idx;
+            if (lane == 0) ok = mbar_wait(sfree_bar(s), sp.phase ^ 1u, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            long long page[2] = {0, 0};
-            int nload = 0;
-            for (int cc = 0; cc < c; ++cc) {
-                while (w.j + cc >= cur_j + 32) {
-                    cur_j += 32;
-                    cur = nxt;
-                    nxt = fetch(cur_j + 32);
+            const uint32_t dst = stage_base + (uint32_t)(2 * s) * kStagePage;
+            if (a.fused) {
+                // a page's codes and scales are one run of 4608 bytes
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kStagePage);
+                    if (nload >= 1)
+                        bulk_load_stream(dst, a.key_cache + page0 * a.page_stride, kStagePage,
+                                         full_bar(s), policy);
+                    if (nload == 2)
+                        bulk_load_stream(dst + kStagePage, a.key_cache + page1 * a.page_stride,
+                                         kStagePage, full_bar(s), policy);
                 }
-                const int entry = __shfl_sync(0xffffffffu, cur, (w.j + cc - cur_j) & 31);
-                if ((long long)(w.j + cc) * kBlockKeys < a.max_context) {
-                    long long pg = entry;
-                    if (pg < 0 || pg >= a.num_pages) {
-                        if (lane == 0) atomicOr(a.status, kStatusBadBlock);
-                        pg = 0;
-                    }
-                    page[cc] = pg;
-                    nload = cc + 1;
+            } else {
+                // codes by bulk copies; scales (pages only 8-byte aligned) by
+                // 8-byte cp.async, two per lane per page
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kPackedPage);
+                    if (nload >= 1)
+                        bulk_load_stream(dst, a.key_cache + page0 * a.page_stride, kPackedPage,
+                                         full_bar(s), policy);
+                    if (nload == 2)
+                        bulk_load_stream(dst + kStagePage, a.key_cache + page1 * a.page_stride,
+                                         kPackedPage, full_bar(s), policy);
                 }
+                for (int cc = 0; cc < nload; ++cc) {
+                    const uint8_t* src = a.key_scales + (cc ? page1 : page0) * a.scale_stride;
+                    const uint32_t sdst = dst + (uint32_t)cc * kStagePage + kPackedPage;
+                    cp_async8(sdst + lane * 8, src + lane * 8);
+                    cp_async8(sdst + (lane + 32) * 8, src + (lane + 32) * 8);
+                }
+                cp_async_arrive(full_bar(s));
             }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kPackedPage);
-                for (int cc = 0; cc < nload; ++cc)
-                    bulk_load_stream(packed_base + (uint32_t)(2 * s + cc) * kPackedPage,
-                                     a.key_cache + page[cc] * a.page_stride, kPackedPage,
-                                     full_bar(s), policy);
-            }
-            for (int cc = 0; cc < nload; ++cc) {
-                const uint8_t* src = a.key_scales + page[cc] * a.scale_stride;
-                const uint32_t dst = scale_base + (uint32_t)(2 * s + cc) * kScalePage;
-                cp_async8(dst + lane * 8, src + lane * 8);
-                cp_async8(dst + (lane + 32) * 8, src + (lane + 32) * 8);
-            }
-            cp_async_arrive(full_bar(s));
             w.advance(c);
             ++it;
             ++k;
+            sp.next(S2);
         }
         if (!ok && lane == 0) {
             for (int t = (k > S2 ? k - S2 : 0); t < k; ++t)
@@ -298,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
         // kg: tile within the request; qk: requests this side has tiles of
-        int it = 0, k = 0, kg = 0, prev_g = -1, qk = 0, slot = 0, last = -1;
+        int it = 0, kg = 0, prev_g = -1, qk = 0, slot = 0, last = -1;
+        RingPos tp;                        // this side's f16 tile
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
@@ -313,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     if (!ok) break;
                     ++qk;
                 }
-                const int tt = mmaw * T2 + k % T2;
-                ok = mbar_wait(deq_bar(tt), (k / T2) & 1, abort_flag, a.status);
+                const int tt = mmaw * T2 + tp.idx;
+                ok = mbar_wait(deq_bar(tt), tp.phase, abort_flag, a.status);
                 if (!ok) break;
                 const int acc = it % kAcc;        // this side's accumulators: it's parity
                 ok = mbar_wait(tempty_bar0 + 8u * acc, ((it / kAcc) & 1) ^ 1, abort_flag, a.status);
@@ -337,15 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 }
                 __syncwarp();
                 last = it;
-                ++k;
+                tp.next(T2);
             }
             w.advance(c);
             ++it;
             ++kg;
         }
         if (!ok && last >= 0) mbar_wait_drain(tfull_bar0 + 8u * (last % kAcc), (last / kAcc) & 1);
-    } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) {
-        // ------------------------------------------------------------ epilogue
+    } else if (egrp >= 0) {
+        // ------------------------------------------------------------ epilogues
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int pg = row >> 6;
@@ -353,10 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, prev_g = -1, len = 0, qk0 = 0, qk1 = 0;
+        int it = 0, prev_g = -1, len = 0, qk = 0;
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
+            if ((it & 1) != egrp) {               // the other side's tile
+                w.advance(c);
+                ++it;
+                continue;
+            }
             if (w.b != prev_g) {
                 prev_g = w.b;
                 len = min(__ldg(a.context_lengths + w.b), a.max_context);
@@ -364,7 +428,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             // the request's last two tiles are the last of each side: each
             // frees its side's q slot
             const bool last_of_side = w.blocks_after(c) <= 2;
-            const int side = it & 1;
             const int acc = it % kAcc;
             ok = mbar_wait(tfull_bar0 + 8u * acc, (it / kAcc) & 1, abort_flag, a.status);
             if (!ok) break;
@@ -382,22 +445,30 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(tempty_bar0 + 8u * acc);
-                if (last_of_side)
-                    mbar_arrive(qempty_bar0 + 8u * (2 * side + ((side ? qk1 : qk0) & 1)));
+                if (last_of_side) mbar_arrive(qempty_bar0 + 8u * (2 * egrp + (qk & 1)));
             }
-            if (last_of_side) {
-                if (side) ++qk1;
-                else ++qk0;
-            }
+            if (last_of_side) ++qk;
             w.advance(c);
             ++it;
         }
     } else if (dgrp >= 0) {
         // ------------------------------------------------------------ dequantisation
-        const int t = threadIdx.x - 32 * (dgrp == 0 ? kFirstDeqWarp : kFirstDeqWarp2);   // row
+        const int t = threadIdx.x - 32 * (dgrp == 0 ? kFirstDeqWarp : kFirstDeqWarp2);
+        // key tiles: thread t expands 16-byte chunk ch = t % 4 (codes 32 ch..32 ch+31,
+        // groups 2 ch and 2 ch + 1) of tile rows row0 + 32 i, row0 = t / 4: a warp
+        // reads 512 contiguous staging bytes per step, and every offset below is
+        // the same for all four rows (row0 + 32 i = row0 mod 8)
+        const int ch = t & 3, row0 = t >> 2;
+        const uint32_t pk_off = (uint32_t)(row0 * kPackedRow + ch * 16);
+        const uint32_t sc_off = (uint32_t)(row0 * kScalesPerRow + ch * 2);
+        const uint32_t tile_off = (uint32_t)((ch >> 1) * kHalfBytes + row0 * 128);
+        uint32_t st_off[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_off[q] = (uint32_t)((((ch & 1) * 4 + q) ^ (row0 & 7)) << 4);
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, k = 0, kg = 0, prev_g = -1, qk = 0;
+        int it = 0, kg = 0, prev_g = -1, qk = 0;
+        RingPos sp, tp;                    // this side's staging slot and f16 tile
         bool ok = true;
         while (!w.done()) {
             const int c = w.cnt();
@@ -435,20 +506,25 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
                     ++qk;
                 }
-                const int s = dgrp * S2 + k % S2, tt = dgrp * T2 + k % T2;
-                ok = mbar_wait(full_bar(s), (k / S2) & 1, abort_flag, a.status);
+                const int s = dgrp * S2 + sp.idx, tt = dgrp * T2 + tp.idx;
+                ok = mbar_wait(full_bar(s), sp.phase, abort_flag, a.status);
                 if (!ok) break;
-                const int pg = t >> 6, r = t & 63;
-                const bool mine = pg < c && (long long)(w.j + pg) * kBlockKeys < a.max_context;
-                ok = mbar_wait(tfree_bar(tt), ((k / T2) & 1) ^ 1, abort_flag, a.status);
+                const bool page_ok[2] = {(long long)w.j * kBlockKeys < a.max_context,
+                                         c > 1 && (long long)(w.j + 1) * kBlockKeys < a.max_context};
+                ok = mbar_wait(tfree_bar(tt), tp.phase ^ 1u, abort_flag, a.status);
                 if (!ok) break;
-                if (mine) {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        smem + L.packed + (2 * s + pg) * kPackedPage + r * kPackedRow);
-                    const uint2 sc = *reinterpret_cast<const uint2*>(
-                        smem + L.scales + (2 * s + pg) * kScalePage + r * kScalesPerRow);
-                    const uint32_t h0 = tile_base + tt * kTileBytes + pg * kPageHalfBytes;
-                    dequant_row(src, sc, h0, h0 + kHalfBytes, r, (r >> 1) & 3);
+                const uint32_t pk = stage_base + (uint32_t)(2 * s) * kStagePage + pk_off;
+                const uint32_t sc = pk - pk_off + kPackedPage + sc_off;
+                const uint32_t dst = tile_base + tt * kTileBytes + tile_off;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {     // tile rows row0 + 32 i: page i / 2
+                    const int pg = i >> 1;
+                    if (!page_ok[pg]) continue;
+                    const uint32_t in_page = (uint32_t)(i & 1) * 32;
+                    const uint4 v = ld_shared_v4(pk + pg * kStagePage + in_page * kPackedRow);
+                    const uint32_t s16 =
+                        ld_shared_u16(sc + pg * kStagePage + in_page * kScalesPerRow);
+                    dequant_chunk(v, s16, dst + (uint32_t)i * 32 * 128, st_off);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -456,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     mbar_arrive(sfree_bar(s));    // staging slot read: refill it
                     mbar_arrive(deq_bar(tt));
                 }
-                ++k;
+                sp.next(S2);
+                tp.next(T2);
             }
             w.advance(c);
             ++it;
