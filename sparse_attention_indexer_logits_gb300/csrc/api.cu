@@ -18,8 +18,8 @@ using namespace pml;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxFp8Stages = 12;
 constexpr int kMaxBf16Stages = 8;
-constexpr int kMaxNvfp4Stages = 16;
-constexpr int kNvfp4Tiles = 4;   // even: two per side
+constexpr int kMaxNvfp4Stages = 32;
+constexpr int kNvfp4Tiles = 6;   // key tiles in tensor memory: three per side
 
 thread_local int g_last_cuda_error = 0;
 
@@ -328,8 +328,8 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
                scale_page_stride_bytes == page_stride_bytes)
                   ? 1
                   : 0;
-    // a few f16 tiles (32 KB each) and as many staging slots (9 KB) as fit;
-    // both split evenly between the kernel's two sides
+    // as many staging slots (9 KB) as fit; both they and the key tiles
+    // split evenly between the kernel's two sides
     a.tiles = kNvfp4Tiles;
     const size_t fixed = nvfp4_smem_bytes(0, a.tiles);
     const size_t per_stage = nvfp4_smem_bytes(1, a.tiles) - fixed;

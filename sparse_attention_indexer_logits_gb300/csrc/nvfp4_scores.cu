@@ -9,33 +9,33 @@
 // of 8; a score is the plain dot product of the dequantised query row and
 // key.)
 //
-// The bf16 engine with a dequantising stage in front of the tensor cores.  A
-// value is an E2M1 code (at most 2 significant bits) times an E4M3 scale (at
-// most 4), so it has at most 6 significant bits and |v| <= 6 * 448 = 2688:
-// exact in f16.  Each tile of two 64-key pages therefore becomes an f16
-// operand with no rounding, and tcgen05.mma kind::f16 accumulates the exact
-// f16 products in fp32.
+// A dequantising stage in front of the tensor cores.  A value is an E2M1 code
+// (at most 2 significant bits) times an E4M3 scale (at most 4), so it has at
+// most 6 significant bits and |v| <= 6 * 448 = 2688: exact in f16.  Each tile
+// of two 64-key pages therefore becomes an f16 operand with no rounding, and
+// tcgen05.mma kind::f16 accumulates the exact f16 products in fp32.  The key
+// tile (A) is written to tensor memory, not shared memory: that halves the
+// shared-memory traffic of a tile, which would otherwise bound the kernel.
 //
 //   (every role comes twice, one copy for each side: the even tiles and the
 //   odd tiles)
-//   warps 0,10 producers: per tile one bulk copy per 4 KB page of packed keys
-//              and 8-byte cp.async copies of the 64 x 8 scale bytes (their
-//              pages need only 8-byte alignment), all completing on the
-//              staging slot's `full` barrier.  Staging slots (9 KB) are many
-//              and are freed as soon as the dequantising warps have read
-//              them; the f16 tiles (32 KB) are few and are freed by the MMA's
-//              commit, so most of the shared memory holds copies in flight.
-//   warps 1,11 MMA issue: 2 K-halves x 4 tcgen05.mma (K = 16) per tile
-//              against the group's rows (padded to N = 16), one commit, into
-//              one of eight TMEM accumulators (16 columns each; a side uses
-//              the four of its parity).
+//   warps 0,10 producers: per tile one bulk copy per page -- 4608 bytes of
+//              codes and scales when the scales follow the codes, else the
+//              4 KB of codes and 8-byte cp.async copies of the 512 scale bytes
+//              (their pages need only 8-byte alignment) -- completing on the
+//              staging slot's `full` barrier, plus a 8-byte record of the
+//              tile's group.  Staging slots (9 KB) fill most of the shared
+//              memory, so many copies are in flight.
+//   warps 1,11 MMA issue: 8 tcgen05.mma (K = 16) per tile, A from tensor
+//              memory, B the group's rows (padded to N = 16) in shared memory,
+//              one commit, into one of eight TMEM accumulators (16 columns
+//              each; a side uses the four of its parity).
 //   warps 2-5, 16-19 epilogues: one key per thread, up to 8 scores per key.
-//   warps 6-9, 12-15 dequantisation: thread t expands one 16-byte chunk
-//              (two groups of 16 codes) of four rows of the tile --
+//   warps 6-9, 12-15 dequantisation: a thread expands one key row --
 //              cvt.rn.f16x2.e2m1x2 per byte and one f16x2 multiply by the
-//              group's scale -- into the 128-byte-swizzled K-major layout the
-//              MMA reads (two K-halves of 64 values); per group of query
-//              rows, whole rows into one of the side's two Q slots.
+//              group's scale -- into its TMEM lane (tcgen05.st, 64 columns);
+//              per group of query rows, the rows into one of the side's two
+//              Q slots (shared memory, 128-byte-swizzled K-major).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,14 +53,12 @@ constexpr int kScalesPerRow = kHeadDim / 16;             // 8
 constexpr int kPackedPage = kBlockKeys * kPackedRow;     // 4096
 constexpr int kScalePage = kBlockKeys * kScalesPerRow;   // 512
 constexpr int kStagePage = kPackedPage + kScalePage;     // 4608: a staged page, codes then scales
-constexpr int kHalfBytes = kTileKeys * 128;              // 16 KB: one f16 K-half of a tile
-constexpr int kTileBytes = 2 * kHalfBytes;               // 32 KB
 constexpr int kQHalfBytes = kN * 128;                    // 2 KB
 constexpr int kQSlotBytes = 2 * kQHalfBytes;             // 4 KB
 // Every role comes twice, one copy for each side of the tile sequence (side
 // p = tile index & 1): one role's per-tile chain (waits, lookups, copy
 // issues, conversions, TMEM loads) is longer than a tile's share of HBM time.
-// Each side has its own half of the staging slots, f16 tiles, accumulators
+// Each side has its own half of the staging slots, key tiles, accumulators
 // and Q slots, so every barrier has one side's roles on it, in tile order.
 constexpr int kProducerWarp = 0;      // and kProducerWarp2
 constexpr int kMmaWarp = 1;           // and kMmaWarp2; warp 1 also allocates TMEM
@@ -71,22 +69,31 @@ constexpr int kMmaWarp2 = 11;
 constexpr int kFirstDeqWarp2 = 12;
 constexpr int kFirstEpiWarp2 = 16;
 constexpr int kThreads = 640;
+constexpr int kRecFirst = 1;
+// Tensor memory: eight accumulators of N = 16 columns (a side uses the four of
+// its parity), then the f16 key tiles, 64 columns each (128 values of a key
+// row, two per column), `tiles` of them.
+constexpr int kAcc = 8;
+constexpr uint32_t kAccCols = kAcc * kN;                 // 128
+constexpr uint32_t kTileCols = kHeadDim / 2;             // 64
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxTiles = (int)((kTmemCols - kAccCols) / kTileCols);   // 6
 
-// Two rings per side: `stages`/2 staging slots of one tile's packed pages and
-// scale bytes (what HBM delivers; deep, so that many copies are in flight) and
-// `tiles`/2 f16 tiles (what the MMA reads; short-lived: freed by the MMA's
-// commit); and two Q slots per side.
+// Shared memory: `stages` staging slots of one tile's two pages (codes then
+// scales, as HBM delivers them; deep, so that many copies are in flight), half
+// of them per side, and two Q slots per side.  The f16 key tiles live in
+// tensor memory (half of `tiles` per side), freed by the MMA's commit.
 struct Nvfp4Layout {
-    uint32_t tile, stage, q, bar, misc, total;
+    uint32_t stage, q, rec, bar, misc, total;
 };
 
 __host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages, int tiles)
 {
     Nvfp4Layout L;
-    L.tile = 0;
-    L.stage = L.tile + (uint32_t)tiles * kTileBytes;             // slot s, page p: 2s + p
+    L.stage = 0;                                               // slot s, page p: 2s + p
     L.q = L.stage + (uint32_t)stages * 2 * kStagePage;
-    L.bar = L.q + 4 * kQSlotBytes;
+    L.rec = L.q + 4 * kQSlotBytes;                             // per staging slot
+    L.bar = L.rec + (uint32_t)stages * 8;
     L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 24) * 8;
     L.total = L.misc + 64;
     return L;
@@ -150,21 +157,21 @@ struct RingPos {
     }
 };
 
-// Dequantise one 16-byte chunk (32 codes: two groups of 16, scales sc & 0xFF
-// and sc >> 8) into four consecutive f16 chunks at dst + off[0..3].
-__device__ __forceinline__ void dequant_chunk(uint4 v, uint32_t sc, uint32_t dst,
-                                              const uint32_t (&off)[4])
+// Dequantise one 16-byte chunk (32 codes: two groups of 16 with scale codes
+// sa, sb) into 16 f16x2 words, byte i -> word i.
+__device__ __forceinline__ void dequant_chunk(uint4 v, uint32_t sa, uint32_t sb,
+                                              uint32_t (&out)[16])
 {
-    const uint32_t sa = e4m3_to_f16x2_dup(sc & 0xFF);
-    const uint32_t sb = e4m3_to_f16x2_dup(sc >> 8);
+    const uint32_t s_a = e4m3_to_f16x2_dup(sa);
+    const uint32_t s_b = e4m3_to_f16x2_dup(sb);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t h[4];
         e2m1x8_to_f16x2x4(w[q], h);
-        const uint32_t s2 = q < 2 ? sa : sb;
-        st_shared_v4(dst + off[q], mul_f16x2(h[0], s2), mul_f16x2(h[1], s2), mul_f16x2(h[2], s2),
-                     mul_f16x2(h[3], s2));
+        const uint32_t s2 = q < 2 ? s_a : s_b;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) out[4 * q + b] = mul_f16x2(h[b], s2);
     }
 }
 
@@ -179,8 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     const Nvfp4Layout L = nvfp4_layout(S, T);
 
     const uint32_t base = smem_addr(smem);
-    const uint32_t tile_base = base + L.tile;
     const uint32_t stage_base = base + L.stage;
+    // per staging slot, written by the producer before the slot's `full`
+    // arrival: {group b, kRecFirst if the side's first tile of b}, or {-1, 0}
+    // after the side's last tile
+    const uint32_t rec_base = base + L.rec;
     const uint32_t q_base = base + L.q;
     const uint32_t bar = base + L.bar;
     auto full_bar = [&](int s) { return bar + 8u * s; };                  // staging landed
@@ -204,8 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                      : (warp >= kFirstDeqWarp2 && warp < kFirstDeqWarp2 + 4) ? 1 : -1;
     const int egrp = (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) ? 0
                      : warp >= kFirstEpiWarp2 ? 1 : -1;
-    constexpr int kAcc = 8;               // accumulators of N = 16 columns in flight
-    constexpr uint32_t kTmemCols = kAcc * kN;
 
     if (warp == kProducerWarp) {
         const long long total = warp_total_blocks(a.context_lengths, a.groups);
@@ -267,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 ++it;
                 continue;
             }
-            if (w.b != prev_g) {
+            const bool first = w.b != prev_g;
+            if (first) {
                 int req = __ldg(a.requests + w.b);
                 if (req < 0 || req >= a.num_requests) {
                     if (lane == 0) atomicOr(a.status, kStatusBadRequest);
@@ -309,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const uint32_t dst = stage_base + (uint32_t)(2 * s) * kStagePage;
+            if (lane == 0) st_shared_v2_s32(rec_base + 8u * s, w.b, first ? kRecFirst : 0);
             if (a.fused) {
                 // a page's codes and scales are one run of 4608 bytes
                 if (lane == 0) {
@@ -344,6 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             ++it;
             ++k;
             sp.next(S2);
+        }
+        if (ok) {
+            // the end mark, in the next slot
+            const int s = prod * S2 + sp.idx;
+            if (lane == 0) ok = mbar_wait(sfree_bar(s), sp.phase ^ 1u, abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) {
+                if (lane == 0) {
+                    st_shared_v2_s32(rec_base + 8u * s, -1, 0);
+                    mbar_arrive_expect_tx(full_bar(s), 0u);
+                }
+                if (!a.fused) cp_async_arrive(full_bar(s));
+            }
         }
         if (!ok && lane == 0) {
             for (int t = (k > S2 ? k - S2 : 0); t < k; ++t)
@@ -381,15 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t d = tmem_base + (uint32_t)(acc * kN);
+                    const uint32_t at = tmem_base + kAccCols + (uint32_t)tt * kTileCols;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint64_t ad =
-                            smem_desc_sw128(tile_base + tt * kTileBytes + h * kHalfBytes);
                         const uint64_t bd =
                             smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, (h | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)   // K = 16: 8 columns of A
+                            mma_f16_tmem_a(d, at + 8u * (4 * h + kk), bd + 2u * kk, idesc,
+                                           (h | kk) ? 1u : 0u);
                     }
                     mma_commit(tfull_bar0 + 8u * acc);
                     mma_commit(tfree_bar(tt));    // the tile may be rewritten once these complete
@@ -454,90 +477,87 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
     } else if (dgrp >= 0) {
         // ------------------------------------------------------------ dequantisation
         const int t = threadIdx.x - 32 * (dgrp == 0 ? kFirstDeqWarp : kFirstDeqWarp2);
-        // key tiles: thread t expands 16-byte chunk ch = t % 4 (codes 32 ch..32 ch+31,
-        // groups 2 ch and 2 ch + 1) of tile rows row0 + 32 i, row0 = t / 4: a warp
-        // reads 512 contiguous staging bytes per step, and every offset below is
-        // the same for all four rows (row0 + 32 i = row0 mod 8)
-        const int ch = t & 3, row0 = t >> 2;
-        const uint32_t pk_off = (uint32_t)(row0 * kPackedRow + ch * 16);
-        const uint32_t sc_off = (uint32_t)(row0 * kScalesPerRow + ch * 2);
-        const uint32_t tile_off = (uint32_t)((ch >> 1) * kHalfBytes + row0 * 128);
-        uint32_t st_off[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) st_off[q] = (uint32_t)((((ch & 1) * 4 + q) ^ (row0 & 7)) << 4);
-        Walk w;
-        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, kg = 0, prev_g = -1, qk = 0;
+        // key tiles: a warp may reach only its own quarter of the TMEM lanes,
+        // so the thread expands tile row (key) 32 * (warp % 4) + lane into that
+        // lane: page row / 64, row row % 64 of it
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t row_off = (uint32_t)((row >> 6) * kStagePage + (row & 63) * kPackedRow);
+        const uint32_t sc_row_off =
+            (uint32_t)((row >> 6) * kStagePage + kPackedPage + (row & 63) * kScalesPerRow);
+        const uint32_t lane_tmem = tmem_base + ((uint32_t)(quad * 32) << 16) + kAccCols;
+        int qk = 0;
         RingPos sp, tp;                    // this side's staging slot and f16 tile
         bool ok = true;
-        while (!w.done()) {
-            const int c = w.cnt();
-            if (w.b != prev_g) {
-                kg = 0;
-                prev_g = w.b;
-            }
-            if ((it & 1) == dgrp) {
-                if (kg < 2) {
-                    // this side's first tile of the request: its query rows into
-                    // this side's next Q slot (rows G..15 zero)
-                    const int slot = 2 * dgrp + (qk & 1);
-                    ok = mbar_wait(qempty_bar0 + 8u * slot, ((qk >> 1) & 1) ^ 1, abort_flag,
-                                   a.status);
-                    if (!ok) break;
-                    const uint32_t qh0 = q_base + slot * kQSlotBytes;
-                    if (t < G) {
-                        const long long qrow = (long long)w.b * G + t;
-                        const uint4* src =
-                            reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
-                        const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2),
-                                             __ldg(src + 3)};
-                        const uint2 sc = __ldg(
-                            reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
-                        dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
-                    } else if (t < kN) {
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            st_shared_v4(qh0 + sw128(t, ch), 0u, 0u, 0u, 0u);
-                            st_shared_v4(qh0 + kQHalfBytes + sw128(t, ch), 0u, 0u, 0u, 0u);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
-                    ++qk;
-                }
-                const int s = dgrp * S2 + sp.idx, tt = dgrp * T2 + tp.idx;
+        while (true) {
+            const int s = dgrp * S2 + sp.idx, tt = dgrp * T2 + tp.idx;
+            // both waits issued before either result is needed
+            const bool got_full = mbar_try_wait(full_bar(s), sp.phase);
+            const bool got_tile = mbar_try_wait(tfree_bar(tt), tp.phase ^ 1u);
+            if (!got_full) {
                 ok = mbar_wait(full_bar(s), sp.phase, abort_flag, a.status);
                 if (!ok) break;
-                const bool page_ok[2] = {(long long)w.j * kBlockKeys < a.max_context,
-                                         c > 1 && (long long)(w.j + 1) * kBlockKeys < a.max_context};
-                ok = mbar_wait(tfree_bar(tt), tp.phase ^ 1u, abort_flag, a.status);
+            }
+            const int2 rec = ld_shared_v2_s32(rec_base + 8u * s);
+            if (rec.x < 0) break;                 // the producer's end mark
+            if (rec.y & kRecFirst) {
+                // this side's first tile of group rec.x: its query rows into
+                // this side's next Q slot (rows G..15 zero)
+                const int slot = 2 * dgrp + (qk & 1);
+                ok = mbar_wait(qempty_bar0 + 8u * slot, ((qk >> 1) & 1) ^ 1, abort_flag, a.status);
                 if (!ok) break;
-                const uint32_t pk = stage_base + (uint32_t)(2 * s) * kStagePage + pk_off;
-                const uint32_t sc = pk - pk_off + kPackedPage + sc_off;
-                const uint32_t dst = tile_base + tt * kTileBytes + tile_off;
+                const uint32_t qh0 = q_base + slot * kQSlotBytes;
+                if (t < G) {
+                    const long long qrow = (long long)rec.x * G + t;
+                    const uint4* src = reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
+                    const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2),
+                                         __ldg(src + 3)};
+                    const uint2 sc = __ldg(
+                        reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
+                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
+                } else if (t < kN) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {     // tile rows row0 + 32 i: page i / 2
-                    const int pg = i >> 1;
-                    if (!page_ok[pg]) continue;
-                    const uint32_t in_page = (uint32_t)(i & 1) * 32;
-                    const uint4 v = ld_shared_v4(pk + pg * kStagePage + in_page * kPackedRow);
-                    const uint32_t s16 =
-                        ld_shared_u16(sc + pg * kStagePage + in_page * kScalesPerRow);
-                    dequant_chunk(v, s16, dst + (uint32_t)i * 32 * 128, st_off);
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        st_shared_v4(qh0 + sw128(t, c8), 0u, 0u, 0u, 0u);
+                        st_shared_v4(qh0 + kQHalfBytes + sw128(t, c8), 0u, 0u, 0u, 0u);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(sfree_bar(s));    // staging slot read: refill it
-                    mbar_arrive(deq_bar(tt));
-                }
-                sp.next(S2);
-                tp.next(T2);
+                if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
+                ++qk;
             }
-            w.advance(c);
-            ++it;
-            ++kg;
+            if (!got_tile) {
+                ok = mbar_wait(tfree_bar(tt), tp.phase ^ 1u, abort_flag, a.status);
+                if (!ok) break;
+            }
+            tc_fence_after();                     // the tile's last MMA read before our stores
+            // every row: a page past the request's end or max_context holds
+            // stale bytes, which only reach accumulator rows the epilogue does
+            // not store
+            const uint32_t slot = stage_base + (uint32_t)(2 * s) * kStagePage;
+            uint4 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = ld_shared_v4(slot + row_off + 16u * c);
+            const uint2 sc = ld_shared_v2_u32(slot + sc_row_off);
+            const uint32_t ta = lane_tmem + (uint32_t)tt * kTileCols;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {         // 16-byte chunk c: columns 16c..16c+15
+                const uint32_t sw = c < 2 ? sc.x : sc.y;
+                uint32_t w16[16];
+                dequant_chunk(v[c], (sw >> (16 * (c & 1))) & 0xFF, (sw >> (16 * (c & 1) + 8)) & 0xFF,
+                              w16);
+                tmem_st16(ta + 16u * c, w16);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sfree_bar(s));        // staging slot read: refill it
+                mbar_arrive(deq_bar(tt));
+            }
+            sp.next(S2);
+            tp.next(T2);
         }
     }
 
@@ -558,6 +578,10 @@ size_t nvfp4_smem_bytes(int stages, int tiles)
 
 cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream)
 {
+    // both rings split between the two sides; the key tiles must fit the
+    // tensor memory the kernel allocates
+    if (a.stages < 2 || (a.stages & 1) || a.tiles < 2 || (a.tiles & 1) || a.tiles > kMaxTiles)
+        return cudaErrorInvalidValue;
     const size_t smem = nvfp4_smem_bytes(a.stages, a.tiles);
     static int configured_device = -1;
     static size_t configured_smem = 0;
