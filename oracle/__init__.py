@@ -77,6 +77,13 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_int,
     ]
     lib.orc_indexer_scores_nvfp4.restype = ctypes.c_int
+    lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e8m0_decode.restype = ctypes.c_double
+    lib.orc_fp4_paged_mqa_logits.argtypes = [
+        P, P, P, i64, P, P, P, i64, ctypes.c_int, ctypes.c_int, P, P, i64, ctypes.c_int,
+        ctypes.c_int,
+    ]
+    lib.orc_fp4_paged_mqa_logits.restype = ctypes.c_int
     return lib
 
 
@@ -120,6 +127,12 @@ def e4m3_decode(code: int) -> float:
 def e2m1_decode(code: int) -> float:
     """Value of a 4-bit E2M1 code (OCP FP4: bias 1, one mantissa bit)."""
     return _load().orc_e2m1_decode(int(code) & 0xF)
+
+
+def e8m0_decode(code: int) -> float:
+    """Value of an E8M0 scale byte (OCP MX shared scale: 2^(code - 127),
+    0xFF NaN)."""
+    return float(_load().orc_e8m0_decode(code))
 
 
 def bf16_decode(bits: int) -> float:
@@ -175,6 +188,50 @@ def fp8_paged_mqa_logits(q, kv_fused, weights, seq_lens, block_table, next_n: in
     rc = _load().orc_fp8_paged_mqa_logits(
         _ptr(q), _ptr(kv), kv.shape[0], _ptr(w), _ptr(sl), _ptr(bt), bt.shape[1], batch,
         next_n, H, _ptr(out), _ptr(mag) if mag is not None else None, out.shape[1],
+        max_context, nthreads or default_threads(),
+    )
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out, mag
+
+
+MXFP4_BLOCK_BYTES = BLOCK_KEYS * (HEAD_DIM // 2 + HEAD_DIM // 32)   # 4352
+
+
+def fp4_paged_mqa_logits(q, q_sf, kv, weights, seq_lens, block_table, next_n: int,
+                         max_context: int | None = None, out=None, with_mag: bool = True,
+                         nthreads: int | None = None):
+    """fp64 MXFP4 logits ``out[b*next_n+t, p] = sum_h w[t,h] * relu(q[t,h].k_p)``
+    over dequantised values, no per-position factor ("flashinfer.attn_scores":
+    math block, first and second bullets, the paragraph after them).
+
+    ``q`` uint8 ``[batch*next_n, 64, 64]`` (E2M1 two to a byte, low nibble
+    first), ``q_sf`` uint8 E8M0 ``[batch*next_n, 64, 4]`` (one per 32
+    values), ``kv`` uint8 ``[num_blocks, 4352]`` (64 keys x 64 code bytes,
+    then 64 x 4 scale bytes), ``weights`` fp32 ``[batch*next_n, 64]``.
+    Written places and ``mag`` as for ``fp8_paged_mqa_logits`` (``mag`` =
+    ``sum_h |w| * |q.k|``)."""
+    q = _c(q, np.uint8)
+    q_sf = _c(q_sf, np.uint8)
+    kv = _c(kv, np.uint8).reshape(-1, MXFP4_BLOCK_BYTES)
+    w = _c(weights, np.float32)
+    sl = _c(seq_lens, np.int32)
+    bt = _c(block_table, np.int32)
+    batch = sl.shape[0]
+    assert q.shape == (batch * next_n, 64, HEAD_DIM // 2), q.shape
+    assert q_sf.shape == (batch * next_n, 64, HEAD_DIM // 32), q_sf.shape
+    assert w.shape == (batch * next_n, 64)
+    if bt.ndim == 1:
+        bt = bt.reshape(batch, -1)
+    if max_context is None:
+        max_context = int(max(1, sl.max(initial=0)))
+    if out is None:
+        out = np.full((batch * next_n, max_context), np.nan, dtype=np.float64)
+    assert out.dtype == np.float64 and out.flags.c_contiguous
+    mag = np.full(out.shape, np.nan, dtype=np.float64) if with_mag else None
+    rc = _load().orc_fp4_paged_mqa_logits(
+        _ptr(q), _ptr(q_sf), _ptr(kv), kv.shape[0], _ptr(w), _ptr(sl), _ptr(bt), bt.shape[1],
+        batch, next_n, _ptr(out), _ptr(mag) if mag is not None else None, out.shape[1],
         max_context, nthreads or default_threads(),
     )
     if rc != 0:

@@ -37,6 +37,22 @@
  *    nibble for odd d; its value is that code times the E4M3 scale number
  *    d/16 of the row (query_scales [rows][8], key_scales [pages][64][8]).
  *    No per-tensor scale appears in that call.
+ *  - MXFP4 paged MQA logits ("flashinfer.attn_scores", second bullet and the
+ *    paragraph after it: MXFP4 block scales folded into the dequantised
+ *    values, one scale per 32-element group on both operands, two FP4 values
+ *    per q byte, num_heads 64 and head_dim 128 only, no per-position factor):
+ *    the scales are the OCP MX shared-scale format E8M0 (value 2^(e - 127),
+ *    0xFF NaN), one per 32 values (sf_vec_size 32); element d of a row is the
+ *    E2M1 code in byte d/2 (low nibble for even d) times scale d/32 of the
+ *    row; q [batch*next_n][64][64] bytes with q_sf [batch*next_n][64][4]; a
+ *    KV block (is_kv_sf_interleaved false) is 64 keys x 64 code bytes
+ *    (4096 B) followed by 64 x 4 scale bytes (256 B): 4352 B per block, the
+ *    same keys-then-scales order as the fp8 kv_fused block.
+ *
+ * MXFP4 arithmetic: a term is a product of two E2M1 values (at most 2
+ * significant bits each) and two powers of two, exact in fp64; the 128-term
+ * sum is exact too unless the group scales of the two rows put terms more
+ * than ~45 binary orders apart.
  *
  * Arithmetic: every product of two e4m3 values is a multiple of 2^-18 below
  * 2^18 in magnitude, and every product of two bf16 values has at most 16
@@ -88,6 +104,14 @@ double orc_e2m1_decode(uint8_t code)
     int m = code & 0x1;
     double mag = e == 0 ? 0.5 * m : ldexp(1.0 + m / 2.0, e - 1);
     return sign ? -mag : mag;
+}
+
+/* OCP MX shared scale E8M0: an unsigned biased exponent, value 2^(e - 127);
+ * 0xFF is NaN. */
+double orc_e8m0_decode(uint8_t code)
+{
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
 }
 
 /* bfloat16 is the upper half of an IEEE binary32 value. */
@@ -456,6 +480,119 @@ int orc_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
     for (int c = 0; c < 256; ++c) J.e4m3[c] = orc_e4m3_decode((uint8_t)c);
     pthread_mutex_init(&J.lock, NULL);
     orc_run_threads(orc_nvfp4_worker, &J, nthreads);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 paged MQA logits                                              */
+/* ------------------------------------------------------------------ */
+
+#define ORC_FP4_HEADS 64
+#define ORC_FP4_ROW_BYTES (ORC_HEAD_DIM / 2)                     /* 64 */
+#define ORC_FP4_ROW_SCALES (ORC_HEAD_DIM / 32)                   /* 4 */
+#define ORC_FP4_BLOCK_CODE_BYTES (ORC_BLOCK_KEYS * ORC_FP4_ROW_BYTES)
+#define ORC_FP4_BLOCK_BYTES (ORC_FP4_BLOCK_CODE_BYTES + ORC_BLOCK_KEYS * ORC_FP4_ROW_SCALES)
+
+typedef struct {
+    const uint8_t* q;
+    const uint8_t* q_sf;
+    const uint8_t* kv;
+    int64_t num_blocks;
+    const float* weights;
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int batch, next_n;
+    double* out;
+    double* mag;
+    int64_t out_stride;
+    int max_context;
+    int next_request;
+    pthread_mutex_t lock;
+} orc_fp4_job;
+
+/* Value of element d of a packed MXFP4 row with its four per-32 scales. */
+static double orc_mxfp4_value(const uint8_t* packed, const uint8_t* scales, int d)
+{
+    const uint8_t byte = packed[d / 2];
+    const uint8_t code = (d % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+    return orc_e2m1_decode(code) * orc_e8m0_decode(scales[d / 32]);
+}
+
+static void orc_fp4_request(orc_fp4_job* J, int b)
+{
+    const int n = J->next_n, H = ORC_FP4_HEADS;
+    const int32_t L = J->seq_lens[b];
+    double qv[ORC_FP4_HEADS][ORC_HEAD_DIM], kv[ORC_HEAD_DIM], x[ORC_FP4_HEADS];
+    if (L <= 0) return;                                  /* rows never written */
+    for (int t = 0; t < n; ++t) {
+        const int64_t row = (int64_t)b * n + t;
+        for (int h = 0; h < H; ++h)
+            for (int d = 0; d < ORC_HEAD_DIM; ++d)
+                qv[h][d] = orc_mxfp4_value(J->q + (row * H + h) * ORC_FP4_ROW_BYTES,
+                                           J->q_sf + (row * H + h) * ORC_FP4_ROW_SCALES, d);
+        const float* w = J->weights + row * H;
+        for (int p = 0; p < L && p < J->max_context; ++p) {
+            /* paging as for fp8: key p is row p%64 of physical block
+             * block_table[b, p/64]; its 4 scales are the (p%64)-th group of 4
+             * bytes after the block's 4096 code bytes */
+            const int64_t phys = J->block_table[J->bt_stride * (int64_t)b + p / ORC_BLOCK_KEYS];
+            const uint8_t* blk = J->kv + phys * ORC_FP4_BLOCK_BYTES;
+            const uint8_t* k = blk + (p % ORC_BLOCK_KEYS) * ORC_FP4_ROW_BYTES;
+            const uint8_t* ks = blk + ORC_FP4_BLOCK_CODE_BYTES + (p % ORC_BLOCK_KEYS) * ORC_FP4_ROW_SCALES;
+            for (int d = 0; d < ORC_HEAD_DIM; ++d) kv[d] = orc_mxfp4_value(k, ks, d);
+            double sum = 0.0, err = 0.0;
+            for (int h = 0; h < H; ++h) {
+                double dot = 0.0;
+                for (int d = 0; d < ORC_HEAD_DIM; ++d) dot += qv[h][d] * kv[d];
+                x[h] = dot;
+            }
+            for (int h = 0; h < H; ++h) {
+                const double rl = x[h] > 0.0 ? x[h] : 0.0;  /* relu per head */
+                sum += (double)w[h] * rl;                   /* then weight and sum */
+                err += fabs((double)w[h]) * fabs(x[h]);
+            }
+            J->out[row * J->out_stride + p] = sum;          /* no per-position factor */
+            if (J->mag) J->mag[row * J->out_stride + p] = err;
+        }
+    }
+}
+
+static void* orc_fp4_worker(void* arg)
+{
+    orc_fp4_job* J = (orc_fp4_job*)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int b = J->next_request++;
+        pthread_mutex_unlock(&J->lock);
+        if (b >= J->batch) break;
+        orc_fp4_request(J, b);
+    }
+    return NULL;
+}
+
+/* MXFP4 logits out[(b*next_n + t) * out_stride + p] = sum_h w[t,h] *
+ * relu(q[t,h] . k_p) over dequantised values, for every request with
+ * seq_lens[b] > 0, every slot t < next_n and every p < min(seq_lens[b],
+ * max_context); nothing else in out is touched.  mag (optional) receives
+ * sum_h |w[t,h]| * |q[t,h] . k_p|.  Returns 0, or -1 on bad arguments. */
+int orc_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv,
+                             int64_t num_blocks, const float* weights, const int32_t* seq_lens,
+                             const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                             double* out, double* mag, int64_t out_stride, int max_context,
+                             int nthreads)
+{
+    if (!q || !q_sf || !kv || !weights || !seq_lens || !block_table || !out) return -1;
+    if (next_n < 1 || batch < 0) return -1;
+    orc_fp4_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.q_sf = q_sf; J.kv = kv; J.num_blocks = num_blocks; J.weights = weights;
+    J.seq_lens = seq_lens; J.block_table = block_table; J.bt_stride = bt_stride;
+    J.batch = batch; J.next_n = next_n; J.out = out; J.mag = mag;
+    J.out_stride = out_stride; J.max_context = max_context;
+    pthread_mutex_init(&J.lock, NULL);
+    orc_run_threads(orc_fp4_worker, &J, nthreads);
     pthread_mutex_destroy(&J.lock);
     return 0;
 }

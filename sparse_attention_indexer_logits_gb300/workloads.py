@@ -515,3 +515,120 @@ def topk_decode(seed: int = 13, k: int = 2048) -> TopkProblem:
     """64 rows of 32768 logits with decode lengths U[1024, 32768], k = 2048."""
     x, sl = topk_logits_input(64, 1, 32768, seed=seed, lo=1024, hi=32768, specials=False)
     return TopkProblem("topk_decode", x, sl, 1, 32768, k)
+
+
+# ---------------------------------------------------------------- MXFP4 logits
+#
+# The MXFP4 variant of the paged logits ("flashinfer.attn_scores", the
+# paragraphs after the math block): q and keys hold E2M1 codes two to a byte
+# with one E8M0 scale byte per 32 values; 64 heads, head_dim 128.  A KV block
+# is 64 keys x 64 code bytes followed by 64 x 4 scale bytes.
+
+MXFP4_ROW_BYTES = HEAD_DIM // 2                                   # 64
+MXFP4_ROW_SCALES = HEAD_DIM // 32                                 # 4
+MXFP4_BLOCK_CODE_BYTES = BLOCK_KEYS * MXFP4_ROW_BYTES              # 4096
+MXFP4_BLOCK_BYTES = MXFP4_BLOCK_CODE_BYTES + BLOCK_KEYS * MXFP4_ROW_SCALES   # 4352
+MXFP4_HEADS = 64
+E8M0_NAN = 0xFF
+
+
+@dataclass
+class Mxfp4Problem:
+    name: str
+    seed: int
+    next_n: int
+    q: np.ndarray            # uint8 [B*n, 64, 64] packed E2M1
+    q_sf: np.ndarray         # uint8 [B*n, 64, 4] E8M0
+    kv: np.ndarray           # uint8 [num_blocks, 4352]
+    weights: np.ndarray      # float32 [B*n, 64]
+    seq_lens: np.ndarray     # int32 [B]
+    block_table: np.ndarray  # int32 [B, width]
+    max_context: int
+
+    num_heads = MXFP4_HEADS
+
+    @property
+    def batch(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv.shape[0])
+
+    @property
+    def positions(self) -> int:
+        return int(np.maximum(self.seq_lens, 0).sum())
+
+    def algorithmic_bytes(self, out_bytes: int = 2) -> int:
+        """Bytes moved once: every valid key (64 code + 4 scale bytes), one
+        block-table entry per block, each request's q rows, scales and weights
+        and its length, and the logits written (bf16 by default)."""
+        n, H = self.next_n, MXFP4_HEADS
+        total = 0
+        for L in self.seq_lens.tolist():
+            if L <= 0:
+                total += 4
+                continue
+            total += L * (MXFP4_ROW_BYTES + MXFP4_ROW_SCALES) + blocks_for(L) * 4
+            total += n * H * (MXFP4_ROW_BYTES + MXFP4_ROW_SCALES + 4) + 4 + n * L * out_bytes
+        return total
+
+
+def random_e8m0(g: np.random.Generator, shape, lo_exp: int = -4, hi_exp: int = 4) -> np.ndarray:
+    """E8M0 scale bytes for 2^lo_exp .. 2^hi_exp (bias 127), drawn as bytes."""
+    return (127 + g.integers(lo_exp, hi_exp, size=shape, endpoint=True)).astype(np.uint8)
+
+
+def mxfp4_problem(name: str, seq_lens, next_n: int, seed: int, *, poison: bool = True,
+                  g: np.random.Generator | None = None, block_table: np.ndarray | None = None,
+                  num_blocks: int | None = None, max_context: int | None = None,
+                  lo_exp: int = -4, hi_exp: int = 4) -> Mxfp4Problem:
+    """An MXFP4 paged problem.  Drawing order: page permutation -> q codes ->
+    q scales -> key codes -> key scales -> weights.  Code bytes are uniform on
+    0..255 (every E2M1 code, -0 included).  With ``poison``, key rows past a
+    request's length and blocks no request uses carry NaN (0xFF) scales."""
+    g = g or rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    B = seq_lens.shape[0]
+    nbs = [blocks_for(L) for L in seq_lens.tolist()]
+    need = sum(nbs)
+    if block_table is None:
+        perm = g.permutation(need).astype(np.int32)
+        num_blocks = need + (1 if poison else 0)
+        width = max(1, max(nbs, default=1))
+        bt = np.full((B, width), need if poison else 0, dtype=np.int32)
+        off = 0
+        for b, nb in enumerate(nbs):
+            bt[b, :nb] = perm[off:off + nb]
+            off += nb
+    else:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        assert num_blocks is not None
+    rows = B * next_n
+    H = MXFP4_HEADS
+    q = g.integers(0, 256, size=(rows, H, MXFP4_ROW_BYTES), dtype=np.uint8)
+    q_sf = random_e8m0(g, (rows, H, MXFP4_ROW_SCALES), lo_exp, hi_exp)
+    codes = g.integers(0, 256, size=(num_blocks, BLOCK_KEYS, MXFP4_ROW_BYTES), dtype=np.uint8)
+    k_sf = random_e8m0(g, (num_blocks, BLOCK_KEYS, MXFP4_ROW_SCALES), lo_exp, hi_exp)
+    weights = (g.standard_normal((rows, H), dtype=np.float32) / np.float32(8.0)).astype(np.float32)
+    if poison:
+        used = np.zeros(num_blocks, dtype=bool)
+        for b, (L, nb) in enumerate(zip(seq_lens.tolist(), nbs)):
+            used[bt[b, :nb]] = True
+            if nb and L % BLOCK_KEYS:
+                k_sf[bt[b, nb - 1], L % BLOCK_KEYS:, :] = E8M0_NAN
+        k_sf[~used] = E8M0_NAN
+    kv = np.empty((num_blocks, MXFP4_BLOCK_BYTES), dtype=np.uint8)
+    kv[:, :MXFP4_BLOCK_CODE_BYTES] = codes.reshape(num_blocks, -1)
+    kv[:, MXFP4_BLOCK_CODE_BYTES:] = k_sf.reshape(num_blocks, -1)
+    mc = max_context or max(1, int(seq_lens.max(initial=0)))
+    return Mxfp4Problem(name, seed, next_n, q, q_sf, kv, weights, seq_lens, bt, mc)
+
+
+def mxfp4_decode(seed: int = 7, batch: int = 64, lo: int = 1024, hi: int = 32768,
+                 next_n: int = 1, poison: bool = True) -> Mxfp4Problem:
+    """MXFP4 decode: 64 heads, lengths uniform on [lo, hi] (the fp8 decode
+    shape with the MXFP4 cache)."""
+    g = rng(seed)
+    seq_lens = g.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
+    return mxfp4_problem(f"mxfp4_decode_b{batch}", seq_lens, next_n, seed, g=g, poison=poison)

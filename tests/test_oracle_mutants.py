@@ -2,8 +2,8 @@
 
 Each case plants one mistake in a copy of ``oracle/oracle.c`` (a dropped
 term, a wrong sign, index or operand), builds it with gcc on the CPU, and runs
-every pin in ``test_oracle_pins.py`` and ``test_oracle_nvfp4_pins.py``
-against it: at least one pin must fail.
+every pin in ``test_oracle_pins.py``, ``test_oracle_nvfp4_pins.py`` and
+``test_oracle_mxfp4_pins.py`` against it: at least one pin must fail.
 The oracle itself is never modified.
 """
 import inspect
@@ -14,6 +14,7 @@ from concurrent.futures import ThreadPoolExecutor
 import pytest
 
 import oracle
+from tests import test_oracle_mxfp4_pins as mxfp4_pins
 from tests import test_oracle_nvfp4_pins as nvfp4_pins
 from tests import test_oracle_pins as pins
 
@@ -54,13 +55,26 @@ MUTANTS = {
                                    "J->query_scales + (int64_t)g * (ORC_HEAD_DIM / 16)"),
     "e2m1_bias": ("ldexp(1.0 + m / 2.0, e - 1)", "ldexp(1.0 + m / 2.0, e)"),
     "e2m1_subnormal": ("e == 0 ? 0.5 * m :", "e == 0 ? 1.0 * m :"),
+    "e8m0_bias": ("ldexp(1.0, (int)code - 127)", "ldexp(1.0, (int)code - 128)"),
+    "mxfp4_scale_per_16": ("orc_e8m0_decode(scales[d / 32])", "orc_e8m0_decode(scales[(d / 16) % 4])"),
+    "mxfp4_key_scale_row": ("ORC_FP4_BLOCK_CODE_BYTES + (p % ORC_BLOCK_KEYS) * ORC_FP4_ROW_SCALES",
+                            "ORC_FP4_BLOCK_CODE_BYTES + (p / ORC_BLOCK_KEYS) * ORC_FP4_ROW_SCALES"),
+    "mxfp4_q_scale_head_ignored": ("J->q_sf + (row * H + h) * ORC_FP4_ROW_SCALES",
+                                   "J->q_sf + (row * H) * ORC_FP4_ROW_SCALES"),
+    "mxfp4_relu_dropped": ("const double rl = x[h] > 0.0 ? x[h] : 0.0;", "const double rl = x[h];"),
+    "mxfp4_block_bytes": ("J->kv + phys * ORC_FP4_BLOCK_BYTES", "J->kv + phys * ORC_FP4_BLOCK_CODE_BYTES"),
+    "mxfp4_block_table_row_ignored": ("J->block_table[J->bt_stride * (int64_t)b + p / ORC_BLOCK_KEYS]",
+                                      "J->block_table[p / ORC_BLOCK_KEYS]"),
+    "mxfp4_slot_ignored": ("J->q + (row * H + h) * ORC_FP4_ROW_BYTES",
+                           "J->q + ((int64_t)b * n * H + h) * ORC_FP4_ROW_BYTES"),
 }
 
 
 def _pin_functions():
     out = []
     members = (inspect.getmembers(pins, inspect.isfunction) +
-               inspect.getmembers(nvfp4_pins, inspect.isfunction))
+               inspect.getmembers(nvfp4_pins, inspect.isfunction) +
+               inspect.getmembers(mxfp4_pins, inspect.isfunction))
     for name, fn in members:
         if not name.startswith("test_"):
             continue
