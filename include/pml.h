@@ -39,6 +39,7 @@ enum {
 #define PML_STATUS_WAIT_TIMEOUT 1u  /* an in-kernel wait exceeded its limit; that CTA stopped early */
 #define PML_STATUS_BAD_BLOCK 2u     /* a block_table entry was outside [0, num_blocks) */
 #define PML_STATUS_BAD_REQUEST 4u   /* a group's request was outside [0, num_requests) */
+#define PML_STATUS_FP4_INEXACT 8u   /* an MXFP4 value was rounded (see pml_fp4_paged_mqa_logits) */
 
 /* Version of this ABI (major*100 + minor). */
 int pml_version(void);
@@ -216,6 +217,49 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
                              int num_requests, const int32_t* context_lengths,
                              const int32_t* requests, int groups, float* scores,
                              int64_t scores_stride, int max_context, void* stream);
+
+/*
+ * pml_fp4_paged_mqa_logits -- the MXFP4 variant ("flashinfer.attn_scores":
+ * the math block, its two bullets and the paragraph after them: MXFP4 block
+ * scales folded into the dequantised values, one per 32-element group on
+ * both operands; two FP4 values per q byte; 64 heads of 128 only; no
+ * per-position factor; default output bf16).
+ *
+ *   out[b*next_n + t, p] = sum_h w[t,h] * relu(q[t,h] . k_p)
+ *
+ * over values code * 2^(e - 127): code an E2M1 value (element d of a row in
+ * byte d/2, low nibble for even d), e the row's E8M0 scale byte d/32.
+ * Written region and schedule as pml_fp8_paged_mqa_logits.
+ *
+ * q          [batch*next_n, 64, 64] packed E2M1, 16-byte aligned
+ * q_sf       [batch*next_n, 64, 4] E8M0, 4-byte aligned
+ * kv_cache   [num_blocks][4352] bytes, 16-byte aligned: per block 64 keys x
+ *            64 code bytes (4096 B), then 64 x 4 E8M0 scale bytes (256 B)
+ * weights    fp32 [batch*next_n, 64], 4-byte aligned
+ * out        output_dtype PML_DTYPE_BFLOAT16 (the pages' default) or
+ *            PML_DTYPE_FLOAT32, [batch*next_n, out_stride]
+ * workspace  device scratch of at least pml_fp4_workspace_bytes(num_blocks,
+ *            batch, next_n) bytes, 16-byte aligned, owned by the caller and
+ *            not read before it is written; must not be in use by another
+ *            call in flight
+ * batch      <= 65535; next_n 1..4; other arguments as the fp8 call
+ *
+ * Method: every row (a key, or one head of one query slot) is rewritten as
+ * E4M3 values times one power of two, 2^(largest group exponent - 127) --
+ * the key's as the fp8 cache's per-token scale, the query row's folded into
+ * its weight (relu commutes with a positive factor) -- and the fp8 logits
+ * engine runs on the result.  That is exact while a row's four group scales
+ * lie within 8 binades of each other (or the smaller groups' codes are large
+ * enough); otherwise the value is rounded to E4M3 and PML_STATUS_FP4_INEXACT
+ * is set.
+ */
+int64_t pml_fp4_workspace_bytes(int64_t num_blocks, int batch, int next_n);
+int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv_cache,
+                             int64_t num_blocks, const float* weights, const int32_t* seq_lens,
+                             const int32_t* block_table, int64_t bt_stride,
+                             const int32_t* schedule_meta, int num_ctas, void* out,
+                             int64_t out_stride, int output_dtype, int max_context, int batch,
+                             int next_n, void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
  * pml_topk_logits -- the indexer's selection over the logits
