@@ -43,10 +43,21 @@ namespace {
 constexpr int kMxRowBytes = kHeadDim / 2;                      // 64
 constexpr int kMxBlockCodeBytes = kBlockKeys * kMxRowBytes;      // 4096
 
+// Sign bits of four E2M1 codes (the low 16 bits of x, one per nibble) moved
+// to the top bit of four bytes.
+__device__ __forceinline__ uint32_t nibble_signs_to_bytes(uint32_t x)
+{
+    return ((x & 0x0008u) << 4) | ((x & 0x0080u) << 8) | ((x & 0x0800u) << 12) |
+           ((x & 0x8000u) << 16);
+}
+
 // One row: 64 code bytes (four 16-byte chunks, chunk g = group g) and the
 // four E8M0 scale bytes in `sc` (byte g = group g) -> 128 E4M3 bytes in
-// `out` (byte d = element d) and the row's power of two.  Returns false if a
-// value was not exact in E4M3.
+// `out` (byte d = element d) and the row's power of two.  Per group, the
+// E4M3 bytes of the eight E2M1 magnitudes times 2^(e_g - e_max) form a table
+// that one byte permute per four codes reads, the code's low three bits as
+// the index; the sign bit is moved across.  Returns false if a code the row
+// uses was not exact in E4M3.
 __device__ __forceinline__ bool mx_row_to_e4m3(const uint4 (&codes)[4], uint32_t sc,
                                                uint32_t (&out)[32], float& row_scale)
 {
@@ -59,34 +70,36 @@ __device__ __forceinline__ bool mx_row_to_e4m3(const uint4 (&codes)[4], uint32_t
         e_max = max(e_max, e);
     }
     row_scale = nan ? __int_as_float(0x7FC00000) : ldexpf(1.0f, e_max - 127);
-    bool exact = true;
+    uint32_t inexact = 0;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const int e = (int)((sc >> (8 * g)) & 0xFF);
         const float down = ldexpf(1.0f, e - e_max);       // 2^-(e_max - e_g), exact or 0
+        uint32_t lut[2] = {0u, 0u}, bad[2] = {0u, 0u};
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {                   // magnitudes 2pr (low), 2pr+1
+            const uint32_t h2 = e2m1x2_to_f16x2((uint32_t)(((2 * pr + 1) << 4) | (2 * pr)));
+            const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+            const float v0 = __low2float(hv) * down, v1 = __high2float(hv) * down;
+            const __nv_fp8_storage_t b0 = __nv_cvt_float_to_fp8(v0, __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8_storage_t b1 = __nv_cvt_float_to_fp8(v1, __NV_SATFINITE, __NV_E4M3);
+            const bool x0 = __half2float(__half(__nv_cvt_fp8_to_halfraw(b0, __NV_E4M3))) == v0;
+            const bool x1 = __half2float(__half(__nv_cvt_fp8_to_halfraw(b1, __NV_E4M3))) == v1;
+            const int sh = 16 * (pr & 1);
+            lut[pr >> 1] |= ((uint32_t)b0 | ((uint32_t)b1 << 8)) << sh;
+            bad[pr >> 1] |= ((x0 ? 0u : 1u) | ((x1 ? 0u : 1u) << 8)) << sh;
+        }
         const uint32_t w[4] = {codes[g].x, codes[g].y, codes[g].z, codes[g].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {                      // 4 bytes = elements 8 per word
-            uint32_t packed = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {                  // byte i: elements 2i (low), 2i+1
-                const uint32_t h2 = e2m1x2_to_f16x2((w[q] >> (8 * i)) & 0xFF);
-                const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-                const float v0 = __low2float(hv) * down, v1 = __high2float(hv) * down;
-                const __nv_fp8_storage_t b0 = __nv_cvt_float_to_fp8(v0, __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8_storage_t b1 = __nv_cvt_float_to_fp8(v1, __NV_SATFINITE, __NV_E4M3);
-                const __half_raw r0 = __nv_cvt_fp8_to_halfraw(b0, __NV_E4M3);
-                const __half_raw r1 = __nv_cvt_fp8_to_halfraw(b1, __NV_E4M3);
-                exact &= __half2float(__half(r0)) == v0 && __half2float(__half(r1)) == v1;
-                packed |= ((uint32_t)b0 | ((uint32_t)b1 << 8)) << (16 * (i & 1));
-                if (i & 1) {
-                    out[g * 8 + q * 2 + (i >> 1)] = packed;
-                    packed = 0;
-                }
-            }
+        for (int q = 0; q < 4; ++q) {                      // 8 codes -> 8 E4M3 bytes
+            const uint32_t lo = w[q] & 0xFFFFu, hi = w[q] >> 16;
+            const uint32_t sel_lo = lo & 0x7777u, sel_hi = hi & 0x7777u;
+            out[g * 8 + 2 * q] = __byte_perm(lut[0], lut[1], sel_lo) | nibble_signs_to_bytes(lo);
+            out[g * 8 + 2 * q + 1] = __byte_perm(lut[0], lut[1], sel_hi) | nibble_signs_to_bytes(hi);
+            inexact |= __byte_perm(bad[0], bad[1], sel_lo) | __byte_perm(bad[0], bad[1], sel_hi);
         }
     }
-    return exact;
+    return inexact == 0;
 }
 
 __device__ __forceinline__ void store_row(uint8_t* dst, const uint32_t (&out)[32])
@@ -97,7 +110,7 @@ __device__ __forceinline__ void store_row(uint8_t* dst, const uint32_t (&out)[32
         d[c] = make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
 }
 
-// grid (x, batch), 128 threads: two blocks of 64 keys per step.
+// grid (x, batch), 128 threads: two blocks of 64 keys per CTA and step.
 __global__ void __launch_bounds__(128) fp4_transcode_kv_kernel(const Fp4TranscodeArgs a)
 {
     const int b = blockIdx.y;
@@ -146,7 +159,11 @@ cudaError_t launch_fp4_transcode(const Fp4TranscodeArgs& a, int batch, cudaStrea
 {
     if (batch > 65535) return cudaErrorInvalidValue;
     if (batch > 0) {
-        fp4_transcode_kv_kernel<<<dim3(8, batch), 128, 0, stream>>>(a);
+        // one CTA per pair of blocks of the longest possible request (the
+        // loop in the kernel covers the rest past 65535 pairs)
+        const long long pairs = ((long long)blocks_of(a.max_context) + 1) / 2;
+        const unsigned gx = (unsigned)(pairs < 1 ? 1 : pairs > 65535 ? 65535 : pairs);
+        fp4_transcode_kv_kernel<<<dim3(gx, batch), 128, 0, stream>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
