@@ -142,6 +142,31 @@ def test_nvfp4_argument_checks(L):
     assert _nvfp4(L, sc_stride=100) == 1 and _nvfp4(L, bt_stride=2) == 1
 
 
+def _fp4(L, **over):
+    a = dict(q=P, qsf=P, kv=P, nb=4, w=P, sl=P, bt=P, bt_stride=4, meta=None, ctas=0, out=P,
+             out_stride=256, dt=1, mc=256, batch=2, n=1, ws=P, wsb=1 << 20)
+    a.update(over)
+    return L.pml_fp4_paged_mqa_logits(a["q"], a["qsf"], a["kv"], a["nb"], a["w"], a["sl"], a["bt"],
+                                      a["bt_stride"], a["meta"], a["ctas"], a["out"],
+                                      a["out_stride"], a["dt"], a["mc"], a["batch"], a["n"],
+                                      a["ws"], a["wsb"], None)
+
+
+def test_fp4_argument_checks(L):
+    assert _fp4(L, batch=0) == 0
+    assert _fp4(L, dt=7) == 2                         # output type
+    assert _fp4(L, n=0) == 2 and _fp4(L, n=5) == 2
+    assert _fp4(L, batch=70000) == 2
+    assert _fp4(L, qsf=None) == 1 and _fp4(L, ws=None) == 1 and _fp4(L, kv=None) == 1
+    assert _fp4(L, wsb=1000) == 1                     # workspace smaller than needed
+    assert _fp4(L, out_stride=100) == 1 and _fp4(L, bt_stride=2) == 1
+    assert _fp4(L, q=P + 8) == 3 and _fp4(L, qsf=P + 2) == 3 and _fp4(L, kv=P + 8) == 3
+    assert _fp4(L, ws=P + 8) == 3
+    # workspace: the fp8 blocks, then 128 E4M3 bytes and one weight per query row
+    assert L.pml_fp4_workspace_bytes(4, 2, 1) == 4 * 8448 + 2 * 64 * 128 + 2 * 64 * 4
+    assert L.pml_fp4_workspace_bytes(-1, 2, 1) == -1
+
+
 def test_topk_argument_checks(L):
     def topk(**o):
         a = dict(x=P, xs=256, sl=P, batch=2, n=1, mc=256, k=16, idx=P, ids=16, val=None, vs=0)
