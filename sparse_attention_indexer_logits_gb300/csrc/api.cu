@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "fp4_transcode.h"
 #include "pml.h"
 
 namespace {

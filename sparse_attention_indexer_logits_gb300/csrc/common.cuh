@@ -19,7 +19,6 @@ constexpr int kHeadDim = 128;                 // q / key length (elements)
 constexpr int kBlockKeys = 64;                // keys per paged block
 constexpr int kFp8BlockKeyBytes = kBlockKeys * kHeadDim;          // 8192
 constexpr int kFp8BlockBytes = kFp8BlockKeyBytes + kBlockKeys * 4; // 8448: keys, then scales
-constexpr int kMxfp4BlockBytes = kBlockKeys * (kHeadDim / 2 + kHeadDim / 32); // 4352: codes, then scales
 constexpr int kTileKeys = 128;                // MMA M: two blocks
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 constexpr unsigned int kWaitSuspendNs = 1000;   // longest hardware suspension per try_wait
@@ -28,7 +27,6 @@ constexpr unsigned int kWaitSuspendNs = 1000;   // longest hardware suspension p
 constexpr unsigned int kStatusWaitTimeout = 1u;   // an mbarrier wait ran out; the CTA aborted
 constexpr unsigned int kStatusBadBlock = 2u;      // a block/page index outside the cache
 constexpr unsigned int kStatusBadRequest = 4u;    // a group's request outside the block table
-constexpr unsigned int kStatusFp4Inexact = 8u;    // an MXFP4 value E4M3 could not hold exactly
 
 __host__ __device__ __forceinline__ int blocks_of(int32_t len)
 {

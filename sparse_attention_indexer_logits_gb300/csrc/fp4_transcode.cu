@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "fp4_transcode.h"
 #include "kernels.h"
 #include "ptx.cuh"
 

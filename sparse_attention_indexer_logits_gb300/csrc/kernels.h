@@ -69,26 +69,6 @@ struct Nvfp4Args {
                      // one page stride), so one bulk copy brings both
 };
 
-// MXFP4 operands re-encoded for the fp8 logits engine (fp4_transcode.cu).
-struct Fp4TranscodeArgs {
-    const uint8_t* q;              // [q_rows][64] packed E2M1, q_rows = batch*next_n*64
-    const uint8_t* q_sf;           // [q_rows][4] E8M0
-    const float* weights;          // [q_rows]
-    const uint8_t* kv;             // [num_blocks][4352]: 64 x 64 code bytes, then 64 x 4 scales
-    const int32_t* seq_lens;
-    const int32_t* block_table;
-    uint8_t* q8;                   // out: [q_rows][128] E4M3
-    float* w8;                     // out: [q_rows] weights times the rows' powers of two
-    uint8_t* kv8;                  // out: [num_blocks][8448] kv_fused blocks (used ones only)
-    unsigned int* status;
-    long long q_rows;
-    long long bt_stride;
-    long long num_blocks;
-    int max_context;
-};
-
-cudaError_t launch_fp4_transcode(const Fp4TranscodeArgs& a, int batch, cudaStream_t stream);
-
 constexpr int kTopkMax = 4096;     // largest k of the top-k selection
 
 struct TopkArgs {
