@@ -8,7 +8,7 @@ operand mistake in either one shows up as a disagreement.
 Sources: FlashInfer documentation, "flashinfer.attn_scores" (math block, the
 two bullets on the per-head rectifier and on the per-token scale s_p, the
 note on row order) and "flashinfer.sdsa.indexer_scores" (one head: plain dot
-product).
+product), and the MXFP4 variant (the paragraph after the two bullets).
 """
 from __future__ import annotations
 
@@ -76,4 +76,54 @@ def bf16_scores(query, key_pages, block_table, context_lengths, requests, group_
                 key = page[k % BLOCK_KEYS]
                 res[(r, k)] = sum(bf16_exact(int(a)) * bf16_exact(int(c))
                                   for a, c in zip(query[r], key))
+    return res
+
+
+def e2m1_exact(code: int) -> Fraction:
+    """Exact value of a 4-bit E2M1 code: sign bit 3, exponent bits 2..1 (bias
+    1), mantissa bit 0; exponent 0 is subnormal, (m/2) * 2^0."""
+    sign = -1 if code & 0x8 else 1
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return sign * Fraction(m, 2)
+    return sign * (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+
+
+def e8m0_exact(code: int):
+    """Exact value of an E8M0 scale byte, 2^(code - 127) (None for 0xFF)."""
+    return None if code == 0xFF else Fraction(2) ** (code - 127)
+
+
+def _mx_row(packed, scales):
+    """128 exact values of a packed MXFP4 row (element d: byte d/2, low
+    nibble for even d, times scale d/32)."""
+    out = []
+    for d in range(HEAD_DIM):
+        byte = int(packed[d // 2])
+        code = byte & 0xF if d % 2 == 0 else byte >> 4
+        out.append(e2m1_exact(code) * e8m0_exact(int(scales[d // 32])))
+    return out
+
+
+def mxfp4_logits(q, q_sf, kv, weights, seq_lens, block_table, next_n):
+    """Dict ``{(row, p): (Fraction logit, Fraction sum_h |w| |q.k|)}`` of
+    every written MXFP4 logit ("flashinfer.attn_scores": the fp4 variant, no
+    per-position factor).  ``kv``: per block a bytes-like of 4352 bytes, 64
+    rows of 64 code bytes then 64 x 4 scale bytes."""
+    res = {}
+    for b, L in enumerate(seq_lens):
+        for t in range(next_n):
+            row = b * next_n + t
+            qv = [_mx_row(q[row][h], q_sf[row][h]) for h in range(len(weights[row]))]
+            for p in range(int(L)):
+                blk = bytes(kv[int(block_table[b][p // BLOCK_KEYS])])
+                r = p % BLOCK_KEYS
+                kv_row = _mx_row(blk[r * 64:(r + 1) * 64], blk[4096 + 4 * r:4096 + 4 * r + 4])
+                total, mag = Fraction(0), Fraction(0)
+                for h, wv in enumerate(weights[row]):
+                    x = sum(a * c for a, c in zip(qv[h], kv_row))
+                    total += Fraction(float(wv)) * (x if x > 0 else 0)
+                    mag += abs(Fraction(float(wv))) * abs(x)
+                res[(row, p)] = (total, mag)
     return res

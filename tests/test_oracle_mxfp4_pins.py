@@ -3,8 +3,10 @@ block, its two bullets and the paragraph after them -- MXFP4 block scales
 folded into the dequantised values, one per 32-element group on both
 operands, two FP4 values per q byte, 64 heads of 128, no per-position
 factor).  Each pin checks the oracle against something other than its own
-code: the published E8M0 and E2M1 tables, torch's E4M3 cast, and the
-separately pinned fp8 oracle on inputs both formats hold exactly."""
+code: the published E8M0 and E2M1 tables, torch's E4M3 cast, the
+separately pinned fp8 oracle on inputs both formats hold exactly, and an
+exact rational restatement (``oracle/brute.py``) on scales far outside E4M3."""
+import functools
 import json
 import os
 
@@ -12,6 +14,7 @@ import numpy as np
 import torch
 
 import oracle
+from oracle import brute
 from sparse_attention_indexer_logits_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -129,3 +132,25 @@ def test_negative_weights_and_unwritten_places():
     assert (out[np.isfinite(out)] < 0).any() and (out[np.isfinite(out)] > 0).any()
     fin = np.isfinite(out)
     assert (np.abs(out[fin]) <= mag[fin]).all()
+
+
+@functools.lru_cache(maxsize=1)
+def _wide_problem_and_exact():
+    # scales 2^-40 .. 2^40 on both operands: far outside what E4M3 holds
+    p = W.mxfp4_problem("wide", [9, 5], 1, seed=26, poison=False, lo_exp=-40, hi_exp=40)
+    exact = brute.mxfp4_logits(p.q, p.q_sf, p.kv, p.weights, p.seq_lens, p.block_table, 1)
+    return p, exact
+
+
+def test_brute_force_rationals_with_wide_scales():
+    """Against an exact rational restatement (another language, no shared
+    code) on scales spread over 80 binades: every written logit within
+    fp64 rounding of the exact one (the 128-term sums are no longer exact
+    there), and the error scale matches."""
+    p, exact = _wide_problem_and_exact()
+    out, mag = oracle.fp4_paged_mqa_logits(p.q, p.q_sf, p.kv, p.weights, p.seq_lens,
+                                           p.block_table, 1, p.max_context)
+    assert len(exact) == int(np.isfinite(out).sum()) == 14
+    for (row, pos), (val, m) in exact.items():
+        assert abs(out[row, pos] - float(val)) <= 2.0 ** -40 * float(m), (row, pos)
+        assert abs(mag[row, pos] - float(m)) <= 2.0 ** -40 * float(m), (row, pos)
