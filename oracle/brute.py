@@ -43,11 +43,15 @@ def bf16_exact(bits: int) -> Fraction:
 
 
 def fp8_logits(q, kv_fused, weights, seq_lens, block_table, next_n):
-    """Dict ``{(row, p): Fraction}`` of every written logit.
+    """Dict ``{(row, p): (logit, mag)}`` of every written logit, both exact
+    Fractions.
 
-    ``q``: nested lists / arrays of e4m3 codes ``[batch*next_n][H][128]``;
-    ``kv_fused``: per block a bytes-like of 8448 bytes; ``weights`` fp32
-    values ``[batch*next_n][H]``; ``block_table[b][j]`` physical block."""
+    ``mag`` is the size of the terms the logit is made of,
+    ``|s_p| * sum_h |w[row,h]| * |q[row,h] . k_p|``, the quantity the
+    parity tolerance is measured against (1e-3 times it, plus 1e-6).  ``q``: nested lists / arrays of e4m3 codes
+    ``[batch*next_n][H][128]``; ``kv_fused``: per block a bytes-like of 8448
+    bytes; ``weights`` fp32 values ``[batch*next_n][H]``;
+    ``block_table[b][j]`` physical block."""
     res = {}
     for b, L in enumerate(seq_lens):
         for t in range(next_n):
@@ -56,12 +60,13 @@ def fp8_logits(q, kv_fused, weights, seq_lens, block_table, next_n):
                 blk = bytes(kv_fused[int(block_table[b][p // BLOCK_KEYS])])
                 key = blk[(p % BLOCK_KEYS) * HEAD_DIM:(p % BLOCK_KEYS + 1) * HEAD_DIM]
                 (s,) = struct.unpack_from("<f", blk, KEY_BYTES + 4 * (p % BLOCK_KEYS))
-                total = Fraction(0)
+                total, terms = Fraction(0), Fraction(0)
                 for h, wv in enumerate(weights[row]):
                     x = sum(e4m3_exact(int(a)) * e4m3_exact(int(c))
                             for a, c in zip(q[row][h], key))
                     total += Fraction(float(wv)) * max(x, Fraction(0))
-                res[(row, p)] = Fraction(s) * total
+                    terms += abs(Fraction(float(wv))) * abs(x)
+                res[(row, p)] = (Fraction(s) * total, abs(Fraction(s)) * terms)
     return res
 
 

@@ -21,6 +21,15 @@ from tests import test_oracle_pins as pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
+    # the tolerance scale |s_p| * sum_h |w| |x_h| that every fp8 parity check uses
+    "mag_rectified_dot": ("bound += fabs((double)w[h]) * fabs(x[h]);",
+                          "bound += fabs((double)w[h]) * r;"),
+    "mag_weight_sign_kept": ("bound += fabs((double)w[h]) * fabs(x[h]);",
+                             "bound += (double)w[h] * fabs(x[h]);"),
+    "mag_scale_dropped": ("J->mag[row * J->out_stride + p] = fabs(s) * bound;",
+                          "J->mag[row * J->out_stride + p] = bound;"),
+    "mag_extra_factor": ("J->mag[row * J->out_stride + p] = fabs(s) * bound;",
+                         "J->mag[row * J->out_stride + p] = fabs(s) * bound * H;"),
     "relu_dropped": ("double r = x[h] > 0.0 ? x[h] : 0.0;", "double r = x[h];"),
     "relu_after_sum": ("J->out[row * J->out_stride + p] = s * acc;",
                        "J->out[row * J->out_stride + p] = s * (acc > 0.0 ? acc : 0.0);"),

@@ -91,7 +91,7 @@ def test_relu_is_per_head_before_weighted_sum():
         assert out[0, 0] == case["logit"]
         assert out[0, 0] != case["relu_of_sum"]
         b = brute.fp8_logits(q, kv, w, [1], [[0]], 1)
-        assert float(b[(0, 0)]) == case["logit"]
+        assert float(b[(0, 0)][0]) == case["logit"]
 
 
 def test_closed_form_one_hot_q_constant_k():
@@ -168,15 +168,18 @@ def test_closed_form_random_multislot_rows():
 ])
 def test_oracle_matches_exact_brute_force(seed, n, H, lens):
     p = W.fp8_problem("brute", lens, n, H, seed, poison=True, extra_blocks=1)
-    out, _ = oracle.fp8_paged_mqa_logits(p.q, p.kv_fused, p.weights, p.seq_lens,
-                                         p.block_table, next_n=n, max_context=p.max_context)
+    out, mag = oracle.fp8_paged_mqa_logits(p.q, p.kv_fused, p.weights, p.seq_lens,
+                                           p.block_table, next_n=n, max_context=p.max_context)
     ref = brute.fp8_logits(p.q, p.kv_fused, p.weights, p.seq_lens, p.block_table, n)
     written = oracle.fp8_written_mask(p.seq_lens, n, p.max_context)
     assert written.sum() == len(ref)
-    for (r, pos), val in ref.items():
+    for (r, pos), (val, m) in ref.items():
         v = float(val)
         assert abs(out[r, pos] - v) <= 1e-12 * max(abs(v), 1e-30), (r, pos, out[r, pos], v)
+        # the tolerance scale of every fp8 parity check, to the same precision
+        assert m > 0 and abs(mag[r, pos] - float(m)) <= 1e-12 * float(m), (r, pos, mag[r, pos], m)
     assert np.isnan(out[~written]).all()
+    assert np.isnan(mag[~written]).all()
 
 
 def test_scale_factors_out():
@@ -196,7 +199,7 @@ def test_scale_factors_out():
     one, _ = oracle.fp8_paged_mqa_logits(p.q[:2], kv1, p.weights[:2], [70],
                                          p.block_table[:1], next_n=2, max_context=70)
     ref = brute.fp8_logits(p.q[:2], kv1, p.weights[:2], [70], p.block_table[:1], 2)
-    for (r, pos), v in ref.items():
+    for (r, pos), (v, _) in ref.items():
         assert one[r, pos] == pytest.approx(float(v), rel=1e-12)
 
 
