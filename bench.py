@@ -271,12 +271,16 @@ def reduce_over_ranks(seconds: float, positions: int, dist, device):
     return float(tmax.item()), int(psum.item())
 
 
-def config_of(workload, p, world, l2="rotate", copies=3):
+def config_of(workload, p, world, l2="rotate", copies=3, launch="graph"):
     l2_text = (f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)" if l2 == "flush"
                else f"inputs larger than L2: {copies} resident copies of the workload used in "
                     f"rotation, back-to-back launches")
+    launch_text = ("each step launched alone between its own events" if l2 == "flush" else
+                   "the K calls captured into one CUDA graph before the timed region, which "
+                   "replays it" if launch == "graph" else
+                   "the K calls issued from Python inside the timed region")
     cfg = {"workload": WORKLOAD_TEXT.get(workload, workload),
-           "l2": l2_text,
+           "l2": l2_text, "launch": launch_text,
            "parallelism": "replicas" if world == 1 else f"dp{world} (independent batches)"}
     if hasattr(p, "k"):
         cfg.update({"rows": int(p.logits.shape[0]), "k": p.k, "max_context": p.max_context,
@@ -304,6 +308,11 @@ def main():
                     help="rotate: cycle through --copies resident input sets (together larger "
                          "than L2) with back-to-back launches; flush: write 256 MiB between steps")
     ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
+                    help="graph: the K timed calls are captured once into a CUDA graph before "
+                         "the timed region, which replays it (device throughput, no host cost "
+                         "per call); eager: the K calls are issued from Python inside the "
+                         "timed region")
     ap.add_argument("--out-dtype", default="float32", choices=["float32", "bfloat16"],
                     help="fp8 workloads: element type of the logits (the output_dtype option)")
     args = ap.parse_args()
@@ -406,12 +415,23 @@ def main():
         step(sets[i % copies])
     torch.cuda.synchronize()
 
+    graph = None
     if flush is not None:
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     else:
         starts = [torch.cuda.Event(enable_timing=True)]
         ends = [torch.cuda.Event(enable_timing=True)]
+        if args.launch == "graph":
+            # the K calls, captured once: the same kernels and arguments as the
+            # eager loop, without the per-call host work in the timed region
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(args.steps):
+                    step(sets[i % copies])
+            graph.replay()
+            torch.cuda.synchronize()
+            stream = torch.cuda.current_stream()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -422,6 +442,14 @@ def main():
                 starts[i].record(stream)
                 step(sets[0])
                 ends[i].record(stream)
+        elif graph is not None:
+            # a ~1 ms device spin ahead of the start event keeps the GPU busy
+            # while the host submits the graph, so the timed region holds the
+            # K calls and not the graph's launch latency
+            torch.cuda._sleep(2_000_000)
+            starts[0].record(stream)
+            graph.replay()
+            ends[0].record(stream)
         else:
             starts[0].record(stream)
             for i in range(args.steps):
@@ -538,7 +566,7 @@ def main():
                                       else ("f32 logits -> int32 indices" if is_topk
                                             else "bf16 x bf16 -> f32"))),
             "data": "synthetic (seeded generators; no public dataset on the pages)",
-            "config": dict(config_of(args.workload, p, world, args.l2, copies),
+            "config": dict(config_of(args.workload, p, world, args.l2, copies, args.launch),
                            **({"output_dtype": args.out_dtype} if is_fp8 else {})),
             "clocks": clocks.summary(), "gpu_launches": args.steps,
             "e2e": e2e, "roofline": roof,

@@ -273,8 +273,14 @@ int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_
     if (bt_stride < pml_min_block_table_width(max_context)) return PML_ERR_INVALID_ARG;
     const int64_t need = pml_fp4_workspace_bytes(num_blocks, batch, next_n);
     if (workspace_bytes < need) return PML_ERR_INVALID_ARG;
+    // every check of the fp8 engine that follows the re-encoding, made before
+    // anything is launched
+    if (schedule_meta != nullptr && num_ctas == 0) return PML_ERR_INVALID_ARG;
+    if ((long long)batch * next_n * kFp4Heads > 0x7fffffffLL) return PML_ERR_INVALID_ARG;
+    const int out_bytes = output_dtype == PML_DTYPE_BFLOAT16 ? 2 : 4;
     if (!aligned(q, 16) || !aligned(q_sf, 4) || !aligned(kv_cache, 16) || !aligned(weights, 4) ||
-        !aligned(seq_lens, 4) || !aligned(block_table, 4) || !aligned(workspace, 16))
+        !aligned(seq_lens, 4) || !aligned(block_table, 4) || !aligned(workspace, 16) ||
+        !aligned(out, out_bytes) || !aligned(schedule_meta, 4))
         return PML_ERR_ALIGNMENT;
     DeviceInfo dev;
     cudaError_t e = device_info(dev);

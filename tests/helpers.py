@@ -124,7 +124,6 @@ def check_bf16(p: W.Bf16Problem, got: np.ndarray, max_context=None, groups=None)
     if groups is None:
         ref, mag = oracle.indexer_scores_bf16(p.query, p.key_cache, p.page_stride_bytes,
                                               p.block_table, p.context_lengths, p.requests, mc)
-        rows = slice(None)
         got_rows = got
     else:
         groups = np.asarray(groups)
@@ -133,8 +132,6 @@ def check_bf16(p: W.Bf16Problem, got: np.ndarray, max_context=None, groups=None)
                                               p.block_table, p.context_lengths[groups],
                                               p.requests[groups], mc)
         got_rows = got[rsel]
-        rows = rsel
-    _ = rows
     written = ~np.isnan(ref)
     err = np.abs(got_rows.astype(np.float64) - np.where(written, ref, 0.0))
     bound = BF16_REL * np.nan_to_num(mag) + ABS

@@ -162,6 +162,11 @@ def test_fp4_argument_checks(L):
     assert _fp4(L, out_stride=100) == 1 and _fp4(L, bt_stride=2) == 1
     assert _fp4(L, q=P + 8) == 3 and _fp4(L, qsf=P + 2) == 3 and _fp4(L, kv=P + 8) == 3
     assert _fp4(L, ws=P + 8) == 3
+    # the logits engine's own checks come before anything is launched
+    assert _fp4(L, out=P + 1) == 3                    # bf16 out on a 2-byte boundary
+    assert _fp4(L, dt=0, out=P + 2) == 3              # fp32 out on a 4-byte boundary
+    assert _fp4(L, meta=P, ctas=0) == 1               # a schedule without its CTA count
+    assert _fp4(L, meta=P + 2, ctas=4) == 3
     # workspace: the fp8 blocks, then 128 E4M3 bytes and one weight per query row
     assert L.pml_fp4_workspace_bytes(4, 2, 1) == 4 * 8448 + 2 * 64 * 128 + 2 * 64 * 4
     assert L.pml_fp4_workspace_bytes(-1, 2, 1) == -1

@@ -29,14 +29,27 @@ def test_random_schedules(seed):
         assert np.array_equal(got, ref), (B, G)
 
 
+def _blocks_per_cta(meta, seq_lens):
+    """Blocks each CTA's range holds, read off the GPU schedule: the global
+    index of each (request, block) start, differenced."""
+    nb = (np.maximum(seq_lens.astype(np.int64), 0) + 63) // 64
+    prefix = np.concatenate([[0], np.cumsum(nb)])
+    starts = prefix[meta[:, 0]] + meta[:, 1]
+    return np.diff(starts), int(prefix[-1])
+
+
 def test_workload_schedules():
     for p in (W.tiny(), W.decode(), W.mtp(4), W.skewed()):
         for G in (148, 152, 304):
             got = pml.pml_schedule(Hh.dev_tensor(p.seq_lens), G, p.next_n).cpu().numpy()
             ref, total = oracle.schedule(p.seq_lens, G)
             assert np.array_equal(got, ref)
-            sizes = np.diff([0] + [0] * 0) if total == 0 else None
-            _ = sizes
+            # load balance of the persistent grid, on the GPU's own output:
+            # every CTA holds floor(T/G) or ceil(T/G) blocks, T in all
+            sizes, t = _blocks_per_cta(got, p.seq_lens)
+            assert t == total and int(sizes.sum()) == total
+            assert sizes.max() <= -(-total // G) and sizes.min() >= total // G, (G, sizes.min(),
+                                                                                 sizes.max())
 
 
 def test_empty_and_zero_batches():
