@@ -44,6 +44,10 @@ WORKLOAD_TEXT = {
               "U[512,4096]",
     "topk_decode": "indexer top-k selection: 64 logits rows of 32768 (lengths U[1024,32768]), "
                    "k 2048, indices of the largest meaningful logits",
+    "mxfp4_decode": "MXFP4 paged MQA logits, decode shape: batch 64, next_n 1, 64 heads, head_dim "
+                    "128, 64-token blocks (64x64 E2M1 code bytes + 64x4 E8M0 scales), seq_lens "
+                    "U[1024,32768], pages shuffled in a shared pool, codes uniform, scales "
+                    "2^-4..2^4, w ~N(0,1)/8, bf16 out",
     "nvfp4_g8": "single-head NVFP4 indexer_scores: 256 groups of 8 rows, E2M1 codes with E4M3 "
                 "scales per 16 values, pages of 4096 code bytes then 512 scale bytes, "
                 "context_lengths U[0,65536] (8 zeros), fp32 scores [2048, 65536]",
@@ -67,6 +71,8 @@ def make_problem(workload: str, rank: int):
         return W.mtp(next_n=n, seed=(2 if n == 4 else 3) + off, poison=False)
     if workload == "skewed":
         return W.skewed(seed=4 + off)
+    if workload == "mxfp4_decode":
+        return W.mxfp4_decode(seed=7 + off, poison=False)
     if workload == "topk_decode":
         return W.topk_decode(seed=13 + off)
     if workload.startswith("nvfp4_g"):
@@ -81,10 +87,11 @@ def make_problem(workload: str, rank: int):
 # traffic figure stays valid while these are unchanged.
 KERNEL_SOURCES = {
     "fp8_logits_kernel": ("fp8_logits.cuh", "fp8_logits.cu", "fp8_logits_h8.cu", "fp8_logits_h16.cu",
-                          "fp8_logits_h32.cu", "fp8_logits_h64.cu"),
+                          "fp8_logits_h32.cu", "fp8_logits_h64.cu", "window.cuh"),
     "bf16_scores_kernel": ("bf16_scores.cu",),
     "nvfp4_scores_kernel": ("nvfp4_scores.cu",),
     "topk_kernel": ("topk.cu",),
+    "mxfp4_logits_kernel": ("mxfp4_logits.cu", "window.cuh"),
 }
 SHARED_SOURCES = ("common.cuh", "ptx.cuh", "kernels.h")
 
@@ -346,7 +353,8 @@ def main():
     p = make_problem(args.workload, rank)
     from sparse_attention_indexer_logits_gb300 import workloads as W
     is_topk = isinstance(p, W.TopkProblem)
-    is_fp8 = hasattr(p, "next_n")
+    is_mx = isinstance(p, W.Mxfp4Problem)
+    is_fp8 = hasattr(p, "next_n") and not is_mx
     is_nvfp4 = isinstance(p, W.Nvfp4Problem)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
@@ -362,6 +370,19 @@ def main():
             pml.pml_topk_logits(d["x"], d["sl"], p.rows_per_request, p.max_context, p.k,
                                 indices=d["out"], stream=stream)
         kernel = "topk_kernel"
+        bound_name = "hbm"
+    elif is_mx:
+        def device_set():
+            return dict(q=t(p.q), qsf=t(p.q_sf), kv=t(p.kv), w=t(p.weights), sl=t(p.seq_lens),
+                        bt=t(p.block_table),
+                        out=torch.zeros((p.batch * p.next_n, p.max_context), dtype=torch.bfloat16,
+                                        device=dev))
+        sets = [device_set() for _ in range(copies)]
+
+        def step(d, stream=None):
+            pml.pml_fp4_paged_mqa_logits(d["q"], d["qsf"], d["kv"], d["w"], d["sl"], d["bt"],
+                                         d["out"], p.max_context, p.next_n, stream=stream)
+        kernel = "mxfp4_logits_kernel"
         bound_name = "hbm"
     elif is_fp8:
         def device_set():
@@ -484,6 +505,20 @@ def main():
                 d.copy_(h, non_blocking=True)
             step(d0)
             hout.copy_(d0["out"], non_blocking=True)
+    elif is_mx:
+        d0 = sets[0]
+        bufs = [(d0["q"], p.q), (d0["qsf"], p.q_sf), (d0["kv"], p.kv), (d0["w"], p.weights),
+                (d0["sl"], p.seq_lens), (d0["bt"], p.block_table)]
+        inputs = tuple((d, torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) for d, a in bufs)
+        hout = torch.empty(d0["out"].shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for _, h in inputs)
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d, h in inputs:
+                d.copy_(h, non_blocking=True)
+            step(d0)
+            hout.copy_(d0["out"], non_blocking=True)
     elif is_fp8:
         hq, hkv, hw = (torch.from_numpy(a).pin_memory() for a in (p.q, p.kv_fused, p.weights))
         hsl, hbt = torch.from_numpy(p.seq_lens).pin_memory(), torch.from_numpy(p.block_table).pin_memory()
@@ -547,7 +582,7 @@ def main():
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
     alg_bytes = (p.algorithmic_bytes(out_dtype.itemsize) if (is_fp8 and not is_topk)
-                 else p.algorithmic_bytes())
+                 else p.algorithmic_bytes())   # MXFP4: bf16 logits
     achieved_gbs = alg_bytes / avg_launch_s / 1e9
     roof = {"bound": bound_name, "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved_gbs / hbm_peak, "traffic": recorded_traffic(kernel, args.workload),
@@ -562,7 +597,9 @@ def main():
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": (("e4m3 x e4m3 -> f32" + (" -> bf16 out" if out_dtype == torch.bfloat16 else ""))
-                      if is_fp8 else ("nvfp4 (e2m1 x e4m3/16) -> f16 x f16 -> f32" if is_nvfp4
+                      if is_fp8 else
+                      ("mxfp4 (e2m1 x e8m0/32) -> f16 or bf16 x same -> f32 -> bf16 out" if is_mx else
+                       "nvfp4 (e2m1 x e4m3/16) -> f16 x f16 -> f32" if is_nvfp4
                                       else ("f32 logits -> int32 indices" if is_topk
                                             else "bf16 x bf16 -> f32"))),
             "data": "synthetic (seeded generators; no public dataset on the pages)",

@@ -39,7 +39,7 @@ enum {
 #define PML_STATUS_WAIT_TIMEOUT 1u  /* an in-kernel wait exceeded its limit; that CTA stopped early */
 #define PML_STATUS_BAD_BLOCK 2u     /* a block_table entry was outside [0, num_blocks) */
 #define PML_STATUS_BAD_REQUEST 4u   /* a group's request was outside [0, num_requests) */
-#define PML_STATUS_FP4_INEXACT 8u   /* an MXFP4 value was rounded (see pml_fp4_paged_mqa_logits) */
+#define PML_STATUS_FP4_INEXACT 8u   /* MXFP4 scales so far apart that tiny products may have been dropped (see pml_fp4_paged_mqa_logits) */
 
 /* Version of this ABI (major*100 + minor). */
 int pml_version(void);
@@ -232,34 +232,39 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
  * Written region and schedule as pml_fp8_paged_mqa_logits.
  *
  * q          [batch*next_n, 64, 64] packed E2M1, 16-byte aligned
- * q_sf       [batch*next_n, 64, 4] E8M0, 4-byte aligned
+ * q_sf       [batch*next_n, 64, 4] E8M0, 16-byte aligned
  * kv_cache   [num_blocks][4352] bytes, 16-byte aligned: per block 64 keys x
  *            64 code bytes (4096 B), then 64 x 4 E8M0 scale bytes (256 B)
- * weights    fp32 [batch*next_n, 64], 4-byte aligned
+ * weights    fp32 [batch*next_n, 64], 16-byte aligned
  * out        output_dtype PML_DTYPE_BFLOAT16 (the pages' default) or
- *            PML_DTYPE_FLOAT32, [batch*next_n, out_stride]
- * workspace  device scratch of at least pml_fp4_workspace_bytes(num_blocks,
- *            batch, next_n) bytes, 16-byte aligned, owned by the caller and
- *            not read before it is written; must not be in use by another
- *            call in flight
- * batch      <= 65535; next_n 1..4; other arguments as the fp8 call
+ *            PML_DTYPE_FLOAT32, [batch*next_n, out_stride], aligned to its
+ *            element
+ * batch      <= 65535; next_n 1..4; other arguments, the written region and
+ *            the schedule as pml_fp8_paged_mqa_logits (next_n 3 and 4 run
+ *            as two passes over the cache, slots 0-1 then the rest, each
+ *            its own launch on `stream`)
  *
- * Method: every row (a key, or one head of one query slot) is rewritten as
- * E4M3 values times one power of two, 2^(largest group exponent - 127) --
- * the key's as the fp8 cache's per-token scale, the query row's folded into
- * its weight (relu commutes with a positive factor) -- and the fp8 logits
- * engine runs on the result.  That is exact while a row's four group scales
- * lie within 8 binades of each other (or the smaller groups' codes are large
- * enough); otherwise the value is rounded to E4M3 and PML_STATUS_FP4_INEXACT
- * is set.
+ * Method: every row (a key, or one head of one query slot) is split into a
+ * power of two, 2^(E - 127) with E its largest group exponent, and its codes
+ * shifted down by each group's distance to E.  The shifted codes are exact
+ * 16-bit operands (f16 while a row's four scales lie within 23 binades, bf16
+ * up to 132) and the tensor cores form their dot products exactly in fp32;
+ * the key's and the query rows' powers of two are applied afterwards, the
+ * rows' folded into the head weights relative to the slot's largest one.  So
+ * each logit is its exact value up to fp32 rounding of the sums -- a logit
+ * beyond the output type's range is +-inf -- except where a key's and a
+ * query row's scale spreads together exceed 124 binades, when products
+ * smaller than 2^-124 of the two rows' largest may be dropped, or a head's
+ * largest scale lies more than 100 binades below the slot's largest: both
+ * set PML_STATUS_FP4_INEXACT.  An E8M0 NaN scale (0xFF) makes its group
+ * NaN, and a NaN dot product is rectified to 0.
  */
-int64_t pml_fp4_workspace_bytes(int64_t num_blocks, int batch, int next_n);
 int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv_cache,
                              int64_t num_blocks, const float* weights, const int32_t* seq_lens,
                              const int32_t* block_table, int64_t bt_stride,
                              const int32_t* schedule_meta, int num_ctas, void* out,
                              int64_t out_stride, int output_dtype, int max_context, int batch,
-                             int next_n, void* workspace, int64_t workspace_bytes, void* stream);
+                             int next_n, void* stream);
 
 /*
  * pml_topk_logits -- the indexer's selection over the logits

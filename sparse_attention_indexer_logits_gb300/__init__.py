@@ -36,7 +36,7 @@ __all__ = [
     "PmlError", "lib", "library_path", "pml_schedule", "pml_fp8_paged_mqa_logits",
     "pml_fp8_paged_mqa_logits_ex",
     "pml_indexer_scores_bf16", "pml_indexer_scores_nvfp4", "pml_topk_logits",
-    "pml_fp4_paged_mqa_logits", "pml_fp4_workspace_bytes",
+    "pml_fp4_paged_mqa_logits",
     "pml_fp8_paged_mqa_logits_noalloc",
     "pml_device_status",
     "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
@@ -97,10 +97,8 @@ def lib() -> ctypes.CDLL:
         L.pml_indexer_scores_nvfp4.restype = i32
         L.pml_topk_logits.argtypes = [P, i64, P, i32, i32, i32, i32, P, i64, P, i64, P]
         L.pml_topk_logits.restype = i32
-        L.pml_fp4_workspace_bytes.argtypes = [i64, i32, i32]
-        L.pml_fp4_workspace_bytes.restype = i64
         L.pml_fp4_paged_mqa_logits.argtypes = [P, P, P, i64, P, P, P, i64, P, i32, P, i64, i32,
-                                               i32, i32, i32, P, i64, P]
+                                               i32, i32, i32, P]
         L.pml_fp4_paged_mqa_logits.restype = i32
         L.pml_fp8_paged_mqa_logits_noalloc.argtypes = [P, P, i64, P, P, P, i64, i32, P, i64, i32,
                                                        i32, i32, i32, P]
@@ -343,28 +341,18 @@ def pml_indexer_scores_nvfp4(query: torch.Tensor, query_scales: torch.Tensor,
     return scores
 
 
-def pml_fp4_workspace_bytes(num_blocks: int, batch: int, next_n: int) -> int:
-    """Device scratch bytes ``pml_fp4_paged_mqa_logits`` needs."""
-    n = int(lib().pml_fp4_workspace_bytes(int(num_blocks), int(batch), int(next_n)))
-    if n < 0:
-        raise ValueError("bad sizes")
-    return n
-
-
 def pml_fp4_paged_mqa_logits(q: torch.Tensor, q_sf: torch.Tensor, kv_cache: torch.Tensor,
                              weights: torch.Tensor, seq_lens: torch.Tensor,
                              block_table: torch.Tensor, out: torch.Tensor, max_context: int,
-                             next_n: int, workspace: torch.Tensor | None = None,
-                             schedule_meta: torch.Tensor | None = None, num_ctas: int = 0,
-                             stream=None) -> torch.Tensor:
+                             next_n: int, schedule_meta: torch.Tensor | None = None,
+                             num_ctas: int = 0, stream=None) -> torch.Tensor:
     """MXFP4 logits ``out[b*next_n+t, p] = sum_h w[t,h] * relu(q[t,h] . k_p)``.
 
     q uint8 ``[batch*next_n, 64, 64]`` (E2M1 two to a byte), q_sf uint8
     ``[batch*next_n, 64, 4]`` (E8M0, one per 32 values), kv_cache uint8
     ``[num_blocks, 4352]`` (64 keys x 64 code bytes, then 64 x 4 scales),
     weights fp32 ``[batch*next_n, 64]``; out bf16 or fp32 ``[batch*next_n,
-    >= max_context]``; workspace a uint8 CUDA tensor of at least
-    ``pml_fp4_workspace_bytes`` bytes (allocated here if None)."""
+    >= max_context]``."""
     for t, nm in ((q, "q"), (q_sf, "q_sf"), (kv_cache, "kv_cache"), (weights, "weights"),
                   (seq_lens, "seq_lens")):
         _cuda(t, nm)
@@ -375,17 +363,11 @@ def pml_fp4_paged_mqa_logits(q: torch.Tensor, q_sf: torch.Tensor, kv_cache: torc
     batch = seq_lens.numel()
     if tuple(q.shape) != (batch * next_n, 64, 64) or tuple(q_sf.shape) != (batch * next_n, 64, 4):
         raise ValueError("q must be uint8 [batch*next_n, 64, 64], q_sf uint8 [batch*next_n, 64, 4]")
-    num_blocks = kv_cache.numel() // 4352
-    need = pml_fp4_workspace_bytes(num_blocks, batch, next_n)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    _cuda(workspace, "workspace")
     _check(lib().pml_fp4_paged_mqa_logits(
-        _ptr(q), _ptr(q_sf), _ptr(kv_cache), num_blocks, _ptr(weights), _ptr(seq_lens),
-        _ptr(block_table), block_table.stride(0), _ptr(schedule_meta), num_ctas, _ptr(out),
-        out.stride(0), _OUT_DTYPES[out.dtype], max_context, batch, next_n, _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)),
-        "pml_fp4_paged_mqa_logits")
+        _ptr(q), _ptr(q_sf), _ptr(kv_cache), kv_cache.numel() // 4352, _ptr(weights),
+        _ptr(seq_lens), _ptr(block_table), block_table.stride(0), _ptr(schedule_meta), num_ctas,
+        _ptr(out), out.stride(0), _OUT_DTYPES[out.dtype], max_context, batch, next_n,
+        _stream(stream)), "pml_fp4_paged_mqa_logits")
     return out
 
 

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libpml.so")
 
 SOURCES = ["api.cu", "schedule.cu", "fp8_logits.cu", "fp8_logits_h8.cu", "fp8_logits_h16.cu",
            "fp8_logits_h32.cu", "fp8_logits_h64.cu", "bf16_scores.cu", "nvfp4_scores.cu",
-           "topk.cu", "fp4_transcode.cu", "noalloc.cu"]
+           "topk.cu", "mxfp4_logits.cu", "noalloc.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

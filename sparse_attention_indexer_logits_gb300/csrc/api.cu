@@ -9,7 +9,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "fp4_transcode.h"
 #include "pml.h"
 
 namespace {
@@ -20,7 +19,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxFp8Stages = 12;
 constexpr int kMaxBf16Stages = 8;
 constexpr int kMaxNvfp4Stages = 32;
-constexpr int kFp4Heads = 64;   // the MXFP4 variant's only head count
+constexpr int kMaxMxfp4Stages = 24;
 constexpr int kNvfp4Tiles = 6;   // key tiles in tensor memory: three per side
 
 thread_local int g_last_cuda_error = 0;
@@ -243,22 +242,12 @@ int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 
-static int64_t fp4_align16(int64_t x) { return (x + 15) / 16 * 16; }
-
-int64_t pml_fp4_workspace_bytes(int64_t num_blocks, int batch, int next_n)
-{
-    if (num_blocks < 0 || batch < 0 || next_n < 1) return -1;
-    const int64_t q_rows = (int64_t)batch * next_n * kFp4Heads;
-    return fp4_align16(num_blocks * kFp8BlockBytes) + fp4_align16(q_rows * kHeadDim) +
-           fp4_align16(q_rows * 4);
-}
-
 int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv_cache,
                              int64_t num_blocks, const float* weights, const int32_t* seq_lens,
                              const int32_t* block_table, int64_t bt_stride,
                              const int32_t* schedule_meta, int num_ctas, void* out,
                              int64_t out_stride, int output_dtype, int max_context, int batch,
-                             int next_n, void* workspace, int64_t workspace_bytes, void* stream)
+                             int next_n, void* stream)
 {
     if (batch < 0 || num_ctas < 0) return PML_ERR_INVALID_ARG;
     if (output_dtype != PML_DTYPE_FLOAT32 && output_dtype != PML_DTYPE_BFLOAT16)
@@ -266,48 +255,51 @@ int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_
     if (next_n < 1 || next_n > 4) return PML_ERR_UNSUPPORTED;
     if (batch == 0) return PML_OK;
     if (batch > 65535) return PML_ERR_UNSUPPORTED;
-    if (!q || !q_sf || !kv_cache || !weights || !seq_lens || !block_table || !out || !workspace)
+    if (!q || !q_sf || !kv_cache || !weights || !seq_lens || !block_table || !out)
         return PML_ERR_INVALID_ARG;
     if (num_blocks < 1 || num_blocks > 0x7fffffffLL) return PML_ERR_INVALID_ARG;
     if (max_context < 1 || out_stride < max_context) return PML_ERR_INVALID_ARG;
     if (bt_stride < pml_min_block_table_width(max_context)) return PML_ERR_INVALID_ARG;
-    const int64_t need = pml_fp4_workspace_bytes(num_blocks, batch, next_n);
-    if (workspace_bytes < need) return PML_ERR_INVALID_ARG;
-    // every check of the fp8 engine that follows the re-encoding, made before
-    // anything is launched
     if (schedule_meta != nullptr && num_ctas == 0) return PML_ERR_INVALID_ARG;
-    if ((long long)batch * next_n * kFp4Heads > 0x7fffffffLL) return PML_ERR_INVALID_ARG;
     const int out_bytes = output_dtype == PML_DTYPE_BFLOAT16 ? 2 : 4;
-    if (!aligned(q, 16) || !aligned(q_sf, 4) || !aligned(kv_cache, 16) || !aligned(weights, 4) ||
-        !aligned(seq_lens, 4) || !aligned(block_table, 4) || !aligned(workspace, 16) ||
-        !aligned(out, out_bytes) || !aligned(schedule_meta, 4))
+    if (!aligned(q, 16) || !aligned(q_sf, 16) || !aligned(kv_cache, 16) || !aligned(weights, 16) ||
+        !aligned(seq_lens, 4) || !aligned(block_table, 4) || !aligned(out, out_bytes) ||
+        !aligned(schedule_meta, 4))
         return PML_ERR_ALIGNMENT;
     DeviceInfo dev;
     cudaError_t e = device_info(dev);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (num_ctas == 0) num_ctas = dev.sm_count;
 
-    const int64_t q_rows = (int64_t)batch * next_n * kFp4Heads;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    Fp4TranscodeArgs t;
-    t.q = q;
-    t.q_sf = q_sf;
-    t.weights = weights;
-    t.kv = kv_cache;
-    t.seq_lens = seq_lens;
-    t.block_table = block_table;
-    t.kv8 = ws;
-    t.q8 = ws + fp4_align16(num_blocks * kFp8BlockBytes);
-    t.w8 = reinterpret_cast<float*>(t.q8 + fp4_align16(q_rows * kHeadDim));
-    t.status = dev.status;
-    t.q_rows = q_rows;
-    t.bt_stride = bt_stride;
-    t.num_blocks = num_blocks;
-    t.max_context = max_context;
-    e = launch_fp4_transcode(t, batch, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    return pml_fp8_paged_mqa_logits_ex(t.q8, t.kv8, num_blocks, t.w8, seq_lens, block_table,
-                                       bt_stride, schedule_meta, num_ctas, out, out_stride,
-                                       output_dtype, max_context, batch, next_n, kFp4Heads, stream);
+    Mxfp4Args a;
+    a.q = q;
+    a.q_sf = q_sf;
+    a.weights = weights;
+    a.kv = kv_cache;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.schedule_meta = schedule_meta;
+    a.out = out;
+    a.status = dev.status;
+    a.bt_stride = bt_stride;
+    a.out_stride = out_stride;
+    a.num_blocks = num_blocks;
+    a.batch = batch;
+    a.next_n = next_n;
+    a.slot0 = 0;
+    a.max_context = max_context;
+    a.out_bf16 = output_dtype == PML_DTYPE_BFLOAT16 ? 1 : 0;
+    // as many staging slots as fit, for a one-slot and a two-slot pass
+    for (int nn = 1; nn <= 2; ++nn) {
+        const size_t fixed = mxfp4_smem_bytes(nn, 0);
+        const size_t per_stage = mxfp4_smem_bytes(nn, 1) - fixed;
+        if ((size_t)dev.smem_optin < fixed + 2 * per_stage) return PML_ERR_UNSUPPORTED;
+        int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
+        if (stages > kMaxMxfp4Stages) stages = kMaxMxfp4Stages;
+        (nn == 1 ? a.stages : a.stages2) = stages;
+    }
+    e = launch_mxfp4_logits(a, num_ctas, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 
 int pml_topk_logits(const float* logits, int64_t logits_stride, const int32_t* seq_lens, int batch,

@@ -27,6 +27,14 @@ constexpr unsigned int kWaitSuspendNs = 1000;   // longest hardware suspension p
 constexpr unsigned int kStatusWaitTimeout = 1u;   // an mbarrier wait ran out; the CTA aborted
 constexpr unsigned int kStatusBadBlock = 2u;      // a block/page index outside the cache
 constexpr unsigned int kStatusBadRequest = 4u;    // a group's request outside the block table
+// MXFP4 logits: a product of query and key values, or a head weight, may have
+// fallen below the range of its row frames and been dropped (see mxfp4_logits.cu)
+constexpr unsigned int kStatusFp4Inexact = 8u;
+
+// MXFP4 paged cache: a block is 64 keys x 64 code bytes (E2M1, two per
+// byte), then 64 x 4 E8M0 scale bytes (one per 32 values).
+constexpr int kMxfp4Heads = 64;
+constexpr int kMxfp4BlockBytes = kBlockKeys * (kHeadDim / 2 + kHeadDim / 32);   // 4352
 
 __host__ __device__ __forceinline__ int blocks_of(int32_t len)
 {

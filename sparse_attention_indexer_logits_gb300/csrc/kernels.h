@@ -69,6 +69,28 @@ struct Nvfp4Args {
                      // one page stride), so one bulk copy brings both
 };
 
+struct Mxfp4Args {
+    const uint8_t* q;              // [batch*next_n][64 heads][64] packed E2M1
+    const uint8_t* q_sf;           // [batch*next_n][64][4] E8M0
+    const float* weights;          // [batch*next_n][64]
+    const uint8_t* kv;             // [num_blocks][4352]
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    const int32_t* schedule_meta;  // nullptr: computed by each CTA
+    void* out;                     // fp32, or bf16 when out_bf16
+    unsigned int* status;
+    long long bt_stride;
+    long long out_stride;          // elements
+    long long num_blocks;
+    int batch;
+    int next_n;
+    int slot0;                     // first query slot of this pass (set per launch)
+    int max_context;
+    int stages;                    // staging slots of a one-slot pass
+    int stages2;                   // ... of a two-slot pass
+    int out_bf16;
+};
+
 constexpr int kTopkMax = 4096;     // largest k of the top-k selection
 
 struct TopkArgs {
@@ -88,12 +110,15 @@ struct TopkArgs {
 size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
 size_t nvfp4_smem_bytes(int stages, int tiles);
+size_t mxfp4_smem_bytes(int slots_per_pass, int stages);
 
 cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
                               const Fp8Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
                                const Bf16Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream);
+// The MXFP4 logits: one launch per pass of at most two query slots.
+cudaError_t launch_mxfp4_logits(const Mxfp4Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
                             cudaStream_t stream);

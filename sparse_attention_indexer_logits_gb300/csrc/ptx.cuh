@@ -579,6 +579,18 @@ __device__ __forceinline__ uint2 ld_shared_v2_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
 {
     uint16_t v;

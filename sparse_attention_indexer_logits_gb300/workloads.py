@@ -573,6 +573,10 @@ class Mxfp4Problem:
             total += n * H * (MXFP4_ROW_BYTES + MXFP4_ROW_SCALES + 4) + 4 + n * L * out_bytes
         return total
 
+    def algorithmic_flops(self) -> int:
+        """Multiply-adds of the dot products: 2 * n * H * 128 per position."""
+        return int(2 * self.next_n * MXFP4_HEADS * HEAD_DIM * np.maximum(self.seq_lens, 0).sum())
+
 
 def random_e8m0(g: np.random.Generator, shape, lo_exp: int = -4, hi_exp: int = 4) -> np.ndarray:
     """E8M0 scale bytes for 2^lo_exp .. 2^hi_exp (bias 127), drawn as bytes."""
@@ -582,11 +586,17 @@ def random_e8m0(g: np.random.Generator, shape, lo_exp: int = -4, hi_exp: int = 4
 def mxfp4_problem(name: str, seq_lens, next_n: int, seed: int, *, poison: bool = True,
                   g: np.random.Generator | None = None, block_table: np.ndarray | None = None,
                   num_blocks: int | None = None, max_context: int | None = None,
-                  lo_exp: int = -4, hi_exp: int = 4) -> Mxfp4Problem:
+                  lo_exp: int = -4, hi_exp: int = 4, q_exp: tuple | None = None,
+                  k_exp: tuple | None = None) -> Mxfp4Problem:
     """An MXFP4 paged problem.  Drawing order: page permutation -> q codes ->
     q scales -> key codes -> key scales -> weights.  Code bytes are uniform on
-    0..255 (every E2M1 code, -0 included).  With ``poison``, key rows past a
-    request's length and blocks no request uses carry NaN (0xFF) scales."""
+    0..255 (every E2M1 code, -0 included).  Scale exponents are uniform on
+    ``q_exp`` / ``k_exp`` (inclusive (lo, hi) pairs, both ``(lo_exp, hi_exp)``
+    unless given; (-127, 127) is every finite E8M0 value).  With ``poison``,
+    key rows past a request's length and blocks no request uses carry NaN
+    (0xFF) scales."""
+    q_exp = q_exp or (lo_exp, hi_exp)
+    k_exp = k_exp or (lo_exp, hi_exp)
     g = g or rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     B = seq_lens.shape[0]
@@ -607,9 +617,9 @@ def mxfp4_problem(name: str, seq_lens, next_n: int, seed: int, *, poison: bool =
     rows = B * next_n
     H = MXFP4_HEADS
     q = g.integers(0, 256, size=(rows, H, MXFP4_ROW_BYTES), dtype=np.uint8)
-    q_sf = random_e8m0(g, (rows, H, MXFP4_ROW_SCALES), lo_exp, hi_exp)
+    q_sf = random_e8m0(g, (rows, H, MXFP4_ROW_SCALES), *q_exp)
     codes = g.integers(0, 256, size=(num_blocks, BLOCK_KEYS, MXFP4_ROW_BYTES), dtype=np.uint8)
-    k_sf = random_e8m0(g, (num_blocks, BLOCK_KEYS, MXFP4_ROW_SCALES), lo_exp, hi_exp)
+    k_sf = random_e8m0(g, (num_blocks, BLOCK_KEYS, MXFP4_ROW_SCALES), *k_exp)
     weights = (g.standard_normal((rows, H), dtype=np.float32) / np.float32(8.0)).astype(np.float32)
     if poison:
         used = np.zeros(num_blocks, dtype=bool)
@@ -626,9 +636,10 @@ def mxfp4_problem(name: str, seq_lens, next_n: int, seed: int, *, poison: bool =
 
 
 def mxfp4_decode(seed: int = 7, batch: int = 64, lo: int = 1024, hi: int = 32768,
-                 next_n: int = 1, poison: bool = True) -> Mxfp4Problem:
+                 next_n: int = 1, poison: bool = True, **scales) -> Mxfp4Problem:
     """MXFP4 decode: 64 heads, lengths uniform on [lo, hi] (the fp8 decode
-    shape with the MXFP4 cache)."""
+    shape with the MXFP4 cache); ``scales`` as for ``mxfp4_problem``."""
     g = rng(seed)
     seq_lens = g.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
-    return mxfp4_problem(f"mxfp4_decode_b{batch}", seq_lens, next_n, seed, g=g, poison=poison)
+    return mxfp4_problem(f"mxfp4_decode_b{batch}", seq_lens, next_n, seed, g=g, poison=poison,
+                         **scales)

@@ -144,12 +144,11 @@ def test_nvfp4_argument_checks(L):
 
 def _fp4(L, **over):
     a = dict(q=P, qsf=P, kv=P, nb=4, w=P, sl=P, bt=P, bt_stride=4, meta=None, ctas=0, out=P,
-             out_stride=256, dt=1, mc=256, batch=2, n=1, ws=P, wsb=1 << 20)
+             out_stride=256, dt=1, mc=256, batch=2, n=1)
     a.update(over)
     return L.pml_fp4_paged_mqa_logits(a["q"], a["qsf"], a["kv"], a["nb"], a["w"], a["sl"], a["bt"],
                                       a["bt_stride"], a["meta"], a["ctas"], a["out"],
-                                      a["out_stride"], a["dt"], a["mc"], a["batch"], a["n"],
-                                      a["ws"], a["wsb"], None)
+                                      a["out_stride"], a["dt"], a["mc"], a["batch"], a["n"], None)
 
 
 def test_fp4_argument_checks(L):
@@ -157,19 +156,15 @@ def test_fp4_argument_checks(L):
     assert _fp4(L, dt=7) == 2                         # output type
     assert _fp4(L, n=0) == 2 and _fp4(L, n=5) == 2
     assert _fp4(L, batch=70000) == 2
-    assert _fp4(L, qsf=None) == 1 and _fp4(L, ws=None) == 1 and _fp4(L, kv=None) == 1
-    assert _fp4(L, wsb=1000) == 1                     # workspace smaller than needed
+    assert _fp4(L, qsf=None) == 1 and _fp4(L, kv=None) == 1 and _fp4(L, w=None) == 1
     assert _fp4(L, out_stride=100) == 1 and _fp4(L, bt_stride=2) == 1
-    assert _fp4(L, q=P + 8) == 3 and _fp4(L, qsf=P + 2) == 3 and _fp4(L, kv=P + 8) == 3
-    assert _fp4(L, ws=P + 8) == 3
-    # the logits engine's own checks come before anything is launched
+    assert _fp4(L, q=P + 8) == 3 and _fp4(L, kv=P + 8) == 3
+    # query scales and weights arrive by bulk copies: 16-byte aligned
+    assert _fp4(L, qsf=P + 4) == 3 and _fp4(L, w=P + 4) == 3
     assert _fp4(L, out=P + 1) == 3                    # bf16 out on a 2-byte boundary
     assert _fp4(L, dt=0, out=P + 2) == 3              # fp32 out on a 4-byte boundary
     assert _fp4(L, meta=P, ctas=0) == 1               # a schedule without its CTA count
     assert _fp4(L, meta=P + 2, ctas=4) == 3
-    # workspace: the fp8 blocks, then 128 E4M3 bytes and one weight per query row
-    assert L.pml_fp4_workspace_bytes(4, 2, 1) == 4 * 8448 + 2 * 64 * 128 + 2 * 64 * 4
-    assert L.pml_fp4_workspace_bytes(-1, 2, 1) == -1
 
 
 def test_topk_argument_checks(L):
