@@ -43,11 +43,12 @@
 //               cache holds them) into a staging slot and a 32-byte record;
 //               per request the raw query codes, scales and weights of the
 //               pass's slots into one of two Q slots.
-//   warp 1      MMA issue (and TMEM allocation): per sub-tile eight
-//               tcgen05.mma kind::f16 (K = 16) with A = the key tile in
-//               tensor memory, B = the request's query rows in shared memory,
-//               into the owning group's accumulator (64 * NN columns);
-//               commits free the key tile and fill the accumulator.
+//   warps 1, 3  MMA issue (warp 1 also allocates TMEM), the sub-tiles of the
+//               even and the odd groups: per sub-tile eight tcgen05.mma
+//               kind::f16 (K = 16) with A = the key tile in tensor memory,
+//               B = the request's query rows in shared memory, into the
+//               owning group's accumulator (64 * NN columns); commits free
+//               the key tile and fill the accumulator.
 //   warp 2      scout: per sub-tile, the largest scale gap among the keys
 //               below the request's length, read from the staged scale bytes,
 //               which fixes the tile's operand format.
@@ -85,6 +86,7 @@ constexpr int kStageBytes = 2 * kMxfp4BlockBytes;         // 8704: one 128-key s
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kScoutWarp = 2;
+constexpr int kMmaWarp2 = 3;                              // second MMA issuer
 constexpr int kFirstWgWarp = 4;
 constexpr uint32_t kTileCols = kHeadDim / 2;              // 64: two 16-bit values per column
 constexpr uint32_t kTmemCols = 512;
@@ -107,8 +109,9 @@ struct Plan {
     static constexpr int N = kHeads * NN;                  // MMA N: query rows of the pass
     static constexpr int NWG = NN == 1 ? 4 : 2;            // warpgroups
     static constexpr int KPW = NN == 1 ? 1 : 2;            // key tiles per warpgroup
+    static constexpr int APW = 1;                          // accumulators per warpgroup
     static constexpr int kThreads = 32 * kFirstWgWarp + 128 * NWG;
-    static constexpr uint32_t kAccCols = (uint32_t)(NWG * N);    // one accumulator per group
+    static constexpr uint32_t kAccCols = (uint32_t)(NWG * APW * N);
     static constexpr int kKeyTiles = NWG * KPW;
     static_assert(kAccCols + kKeyTiles * kTileCols <= kTmemCols, "tensor memory");
     // one Q slot: the 16-bit operand in both formats (two K halves of N rows
@@ -146,7 +149,7 @@ __host__ __device__ inline Layout layout_of(int stages)
     L.info = L.gap + ((uint32_t)stages * 4 + 15) / 16 * 16;
     L.done = L.info + (uint32_t)P::kKeyTiles * 16;
     L.bar = L.done + 16;
-    L.misc = L.bar + (uint32_t)(3 * stages + 6 + 2 * P::kKeyTiles + 3 * P::NWG) * 8;
+    L.misc = L.bar + (uint32_t)(3 * stages + 6 + 2 * P::kKeyTiles + (2 * P::APW + 1) * P::NWG) * 8;
     L.total = L.misc + 32;
     return L;
 }
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
     const uint32_t ktfull0 = qempty0 + 16;                // key tile written
     const uint32_t ktfree0 = ktfull0 + 8u * P::kKeyTiles; // key tile read by the MMA
     const uint32_t accfull0 = ktfree0 + 8u * P::kKeyTiles;
-    const uint32_t accempty0 = accfull0 + 8u * NWG;
-    const uint32_t wgsync0 = accempty0 + 8u * NWG;       // a group's four warps meet
+    const uint32_t accempty0 = accfull0 + 8u * NWG * P::APW;
+    const uint32_t wgsync0 = accempty0 + 8u * NWG * P::APW;   // a group's four warps meet
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
     int* done_cnt = reinterpret_cast<int*>(smem + L.done);   // per Q slot
@@ -364,11 +367,11 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             mbar_init(ktfull0 + 8u * i, 4);
             mbar_init(ktfree0 + 8u * i, 1);
         }
-        for (int i = 0; i < NWG; ++i) {
+        for (int i = 0; i < NWG * P::APW; ++i) {
             mbar_init(accfull0 + 8u * i, 1);
             mbar_init(accempty0 + 8u * i, 4);
-            mbar_init(wgsync0 + 8u * i, 4);
         }
+        for (int i = 0; i < NWG; ++i) mbar_init(wgsync0 + 8u * i, 4);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -514,12 +517,16 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             __syncwarp();
             st.next(S);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
         // ---------------------------------------------------------------- MMA issue
-        int qc = 0, last_acc = -1;
+        // Issuing a tcgen05.mma takes a thread longer than the tensor pipe
+        // needs to run it at N = 64, so two warps issue: warp 1 the sub-tiles
+        // of the even groups, warp 3 those of the odd ones (k even / odd).
+        const int m = warp == kMmaWarp ? 0 : 1;
+        int last_q = -1, last_acc = -1;
         uint32_t last_ph = 0;
         bool ok = true;
-        for (int k = 0;; ++k) {
+        for (int k = m;; k += 2) {
             const int wg = k % NWG;
             const int i = k / NWG;                        // the group's own sub-tile count
             const int kt = wg * KPW + i % KPW;
@@ -528,13 +535,14 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             const uint4 info = ld_shared_v4(base + L.info + 16u * kt);
             if (info.x & kStageEnd) break;
             const int slot = (int)info.y;
-            if (info.x & kMetaFirst) {
-                ok = mbar_wait(qready0 + 8u * slot, (uint32_t)(qc >> 1) & 1u, abort_flag, a.status);
+            if ((int)info.w != last_q) {
+                // this warp's first sub-tile of the request: its query rows
+                last_q = (int)info.w;
+                ok = mbar_wait(qready0 + 8u * slot, (uint32_t)(last_q >> 1) & 1u, abort_flag, a.status);
                 if (!ok) break;
-                ++qc;
             }
-            const int acc = wg;
-            const uint32_t aph = (uint32_t)i & 1u;
+            const int acc = wg * P::APW + i % P::APW;
+            const uint32_t aph = (uint32_t)(i / P::APW) & 1u;
             ok = mbar_wait(accempty0 + 8u * acc, aph ^ 1u, abort_flag, a.status);
             if (!ok) break;
             tc_fence_after();
@@ -571,7 +579,6 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
         const uint32_t stage_row = (uint32_t)(page * kMxfp4BlockBytes + key * kRowBytes);
         const uint32_t stage_sc = (uint32_t)(page * kMxfp4BlockBytes + kBlockCodeBytes + key * kRowScales);
         const int rot = (row >> 1) & 3;                  // chunk order: distinct banks per warp
-        const uint32_t acc_col = (uint32_t)(wg * N);
         // the group's four warps meet on an mbarrier of their own (one
         // arrival per warp), so that the meeting is bounded like every other
         // wait: a warp that gave up elsewhere cannot hold the others forever
@@ -587,6 +594,7 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
         // the group's sub-tile whose epilogue is still to run
         struct Pending {
             bool has;
+            int acc;
             uint32_t aph;
             int slot, qidx, b, j, len, cnt, E, sub_idx;
             bool last;
@@ -601,7 +609,7 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
         // kDoneAll exactly when every sub-tile of the request in this CTA is
         // done, and the warp whose count completes it frees the slot.
         auto epilogue = [&](const Pending& p) -> bool {
-            if (!mbar_wait(accfull0 + 8u * wg, p.aph, abort_flag, a.status)) return false;
+            if (!mbar_wait(accfull0 + 8u * p.acc, p.aph, abort_flag, a.status)) return false;
             tc_fence_after();
             const uint32_t qs = q0 + p.slot * P::kSlotBytes;
             const int pos = (p.j + page) * kBlockKeys + key;
@@ -609,6 +617,7 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             constexpr int NC = NN * 2;                    // 32-column chunks
             uint32_t buf[2][32];
             uint64_t acc4[4];
+            const uint32_t acc_col = (uint32_t)(p.acc * N);
             tmem_ld32_async(lane_tmem + acc_col, buf[0]);
             tmem_wait_bind32(buf[0]);
 #pragma unroll
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(accempty0 + 8u * wg);
+                mbar_arrive(accempty0 + 8u * p.acc);
                 // Count this warp's part of the sub-tile towards the Q slot's
                 // release.  A sub-tile counts 1 per warp, except the request's
                 // last one (index T-1 of T), whose warps add kDoneAll/4 -
@@ -785,7 +794,8 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
             const int fmt = (tile_gap <= kF16MaxGap && qm.x) ? kFmtF16 : kFmtBf16;
             if (row == 0) {
                 if (tile_gap + qm.y > kExactGapSum) atomicOr(a.status, kStatusFp4Inexact);
-                st_shared_v4(base + L.info + 16u * kt, (uint32_t)meta, (uint32_t)slot, (uint32_t)fmt, 0u);
+                st_shared_v4(base + L.info + 16u * kt, (uint32_t)meta, (uint32_t)slot, (uint32_t)fmt,
+                             (uint32_t)qidx);
             }
             const uint32_t ta = lane_tmem + P::kAccCols + (uint32_t)kt * kTileCols;
             // the row's four 16-byte chunks (group c = chunk c), read in a
@@ -817,7 +827,8 @@ __global__ void __launch_bounds__(Plan<NN>::kThreads, 1) mxfp4_logits_kernel(con
                 break;
             }
             pend.has = true;
-            pend.aph = (uint32_t)i & 1u;
+            pend.acc = wg * P::APW + i % P::APW;
+            pend.aph = (uint32_t)(i / P::APW) & 1u;
             pend.slot = slot;
             pend.qidx = qidx;
             pend.b = (int)r0.x;
