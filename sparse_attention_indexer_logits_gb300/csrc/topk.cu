@@ -9,15 +9,28 @@
 // others with the sign bit set: -NaN < -inf < ... < -0 < +0 < ... < +inf <
 // +NaN), equal values by ascending position.
 //
-// One CTA per row: a radix select, 8 bits per pass over the row, finds the
-// exact key T of the K-th largest candidate (K = min(k, lim)); one more pass
-// collects every key above T, and the first (in position order) of the keys
-// equal to T through a block-wide scan; a bitonic sort of (key, ~position)
-// pairs in shared memory gives the output order.  A row whose candidates fit
-// in the rest of shared memory is read from global memory once and the five
-// passes run on that copy.
+// A row is one cluster of kSlices CTAs; CTA s of the cluster holds the
+// slice [s*chunk, min(lim, (s+1)*chunk)) of the row, chunk = ceil(lim /
+// kSlices), in shared memory when it fits.
+//   1. Radix select of the exact key T of the K-th largest candidate (K =
+//      min(k, lim)), 8 bits per pass: each CTA histograms its slice, and
+//      every CTA sums the kSlices histograms through distributed shared
+//      memory (two histogram buffers, alternating, so one cluster barrier
+//      per pass suffices).
+//   2. Each CTA counts its keys above T and equal to T; after an exchange of
+//      the counts it knows where its candidates go: all its keys above T,
+//      and the first ones equal to T in position order that the slices
+//      before it left over (K - #above in all).
+//   3. Each CTA sorts its candidates, (key, ~position) descending, in its own
+//      shared memory; after a cluster barrier it copies every other CTA's
+//      sorted list next to its own and places each of its candidates at its
+//      rank: its index in its own list plus, for every other list, the
+//      number of entries there that come before it (binary search).
+//      Candidates are distinct, so the ranks are a permutation of 0..K-1.
+// Every CTA of a cluster takes the same path (K is the row's), so they all
+// meet at every cluster barrier; the last one keeps each CTA's shared memory
+// alive until the others are done reading it.
 #include <cuda_runtime.h>
-#include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -26,7 +39,8 @@ namespace pml {
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kSlices = 8;          // CTAs per row (a portable cluster size)
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 // Keys and values stay integer bit patterns throughout: a float register can
@@ -48,27 +62,111 @@ __device__ __forceinline__ unsigned long long pack_cand(uint32_t key, int p)
     return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)p);
 }
 
-// The candidates' bit patterns: from the shared-memory copy of the row when
-// it fits (`cached`), else from global memory.
-struct RowSource {
-    const uint32_t* gx;
-    const uint32_t* sx;
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives; shared-memory writes
+// before it are visible to the cluster after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank)
+{
+    uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    return ra;
+}
+
+// Loads from another CTA's shared memory.  They carry no memory clobber, so
+// that several can be in flight at once; being volatile they stay after the
+// cluster barrier that precedes them, and a later write of this CTA's own
+// shared memory does not alias anything they read.
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr)
+{
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr));
+    return v;
+}
+
+// The slice's candidates: from the shared-memory copy when it fits
+// (`cached`), else from global memory.
+struct SliceSource {
+    const uint32_t* gx;    // the row, position 0
+    const uint32_t* sx;    // the copy, slice position 0
+    int s0;
     bool cached;
     __device__ __forceinline__ uint32_t operator()(int p) const
     {
-        return cached ? sx[p] : __ldg(gx + p);
+        return cached ? sx[p - s0] : __ldg(gx + p);
     }
 };
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems)
+// Block-wide exclusive scan of one int per thread (kThreads threads); also
+// returns the total.  Uses `buf` (kWarps ints).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* buf, int& total)
 {
-    __shared__ unsigned int hist[256];
-    __shared__ unsigned long long cand[kTopkMax];
-    __shared__ int warp_sums[kWarps];
-    __shared__ int sel[2];
-    extern __shared__ uint32_t row_cache[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) buf[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int s = buf[w];
+        before += w < warp ? s : 0;
+        total += s;
+    }
+    __syncthreads();
+    return before + incl - v;
+}
 
-    const int row = blockIdx.x;
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems, int sort_cap)
+{
+    __shared__ __align__(16) unsigned int hist[2][256];
+    __shared__ __align__(16) unsigned int merged[256];            // the slices' histograms summed
+    __shared__ int slice_counts[4][kSlices];                      // counts[] of every slice
+    __shared__ int counts[4];        // {above T, equal to T, list offset, list length} of this CTA
+    __shared__ int sel[2];
+    __shared__ int scan_buf[kWarps];
+    extern __shared__ __align__(16) uint8_t dyn[];
+    // dynamic: the sorted list (sort_cap entries), every CTA's lists
+    // (k entries), the slice copy (cache_elems)
+    unsigned long long* own = reinterpret_cast<unsigned long long*>(dyn);
+    unsigned long long* all = own + sort_cap;
+    uint32_t* slice_copy = reinterpret_cast<uint32_t*>(all + a.k);
+
+    const int row = blockIdx.x / kSlices;
+    const uint32_t rank = cluster_rank();
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int b = row / a.next_n, t = row % a.next_n;
@@ -76,36 +174,63 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
     int lim = len > 0 ? min(len - a.next_n + t + 1, a.max_context) : 0;
     if (lim < 0) lim = 0;
     const int K = min(a.k, lim);
+    const int chunk = (lim + kSlices - 1) / kSlices;
+    const int s0 = min(lim, (int)rank * chunk), s1 = min(lim, s0 + chunk);
     const uint32_t* gx =
         reinterpret_cast<const uint32_t*>(a.logits) + (long long)row * a.logits_stride;
-    // one read of the row from global memory when it fits in shared memory
-    const bool cached = lim <= cache_elems;
+    const bool cached = chunk <= cache_elems;
     if (cached) {
-        for (int p = tid; p < lim; p += kThreads) row_cache[p] = __ldg(gx + p);
-        __syncthreads();
+        for (int p = s0 + tid; p < s1; p += kThreads) slice_copy[p - s0] = __ldg(gx + p);
     }
-    const RowSource x{gx, row_cache, cached};
+    const SliceSource x{gx, slice_copy, s0, cached};
 
-    // radix select of the K-th largest key
+    // ---------------------------------------------------------------- 1. radix select
     uint32_t prefix = 0, mask = 0;
     int need = K;
-    for (int shift = 24; shift >= 0 && K > 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+    int buf = 0;
+    for (int shift = 24; shift >= 0 && K > 0; shift -= 8, buf ^= 1) {
+        hist[buf][tid] = 0u;                       // kThreads == 256 bins
+        merged[tid] = 0u;
         __syncthreads();
-        for (int p = tid; p < lim; p += kThreads) {
-            const uint32_t key = order_key(x(p));
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        // four positions per thread per step, loaded before any is counted
+        for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
+            int bins[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                const uint32_t key = p < s1 ? order_key(x(p)) : 0u;
+                bins[u] = (p < s1 && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (bins[u] >= 0) atomicAdd(&hist[buf][bins[u]], 1u);
+        }
+        __syncthreads();
+        cluster_sync();
+        {
+            // the slices' histograms summed in this CTA: thread t adds bins
+            // 8(t%32) .. 8(t%32)+7 of slice t/32 (two 16-byte remote loads per
+            // thread rather than many per thread, as remote loads of one
+            // thread complete one after another)
+            const int r = tid >> 5, b8 = (tid & 31) * 8;
+            const uint32_t src = remote_addr(&hist[buf][b8], (uint32_t)r);
+            const uint4 lo = ld_cluster_v4(src), hi = ld_cluster_v4(src + 16);
+            atomicAdd(&merged[b8 + 0], lo.x); atomicAdd(&merged[b8 + 1], lo.y);
+            atomicAdd(&merged[b8 + 2], lo.z); atomicAdd(&merged[b8 + 3], lo.w);
+            atomicAdd(&merged[b8 + 4], hi.x); atomicAdd(&merged[b8 + 5], hi.y);
+            atomicAdd(&merged[b8 + 6], hi.z); atomicAdd(&merged[b8 + 7], hi.w);
         }
         __syncthreads();
         if (warp == 0) {
-            // lane l holds bins 255-8l .. 248-8l (descending); the first lane whose
-            // inclusive count reaches `need` holds the bin of the K-th largest
-            unsigned c[8], s = 0;
+            // lane l sums bins 255-8l .. 248-8l over the slices (descending);
+            // the first lane whose inclusive count reaches `need` holds the
+            // bin of the K-th largest
+            unsigned c[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = hist[255 - (lane * 8 + j)];
-                s += c[j];
-            }
+            for (int j = 0; j < 8; ++j) c[j] = merged[255 - (lane * 8 + j)];
+            unsigned s = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s += c[j];
             unsigned incl = s;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -132,97 +257,247 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
         need -= sel[1];
         prefix |= (uint32_t)sel[0] << shift;
         mask |= 255u << shift;
-        __syncthreads();
     }
+    // T = prefix; the K-th largest key; `need` keys equal to T are taken
 
-    // collect: every key above T, then the first `need` keys equal to T
-    const int n_above = K - need;
+    // ---------------------------------------------------------------- 2. this CTA's candidates
+    int n_above = 0, n_equal = 0;
     if (K > 0) {
+        for (int p = s0 + tid; p < s1; p += kThreads) {
+            const uint32_t key = order_key(x(p));
+            n_above += key > prefix;
+            n_equal += key == prefix;
+        }
+    }
+    int tot_above, tot_equal;
+    (void)block_exclusive_scan(n_above, scan_buf, tot_above);
+    (void)block_exclusive_scan(n_equal, scan_buf, tot_equal);
+    if (tid == 0) {
+        counts[0] = tot_above;
+        counts[1] = tot_equal;
+    }
+    __syncthreads();
+    cluster_sync();
+    // the slices before this one: their keys above T and equal to T
+    if (tid < 2 * kSlices)
+        slice_counts[tid / kSlices][tid % kSlices] =
+            (int)ld_cluster_u32(remote_addr(&counts[tid / kSlices], (uint32_t)(tid % kSlices)));
+    __syncthreads();
+    int above_before = 0, equal_before = 0;
+#pragma unroll
+    for (int r = 0; r < kSlices; ++r) {
+        if (r < (int)rank) {
+            above_before += slice_counts[0][r];
+            equal_before += slice_counts[1][r];
+        }
+    }
+    // keys equal to T taken by this slice: the first take_e of its own
+    const int take_e = K > 0 ? max(0, min(tot_equal, need - equal_before)) : 0;
+    const int m = K > 0 ? tot_above + take_e : 0;          // this CTA's candidates
+    // its list starts after the lists of the slices before it
+    const int taken_before = above_before + min(equal_before, need);
+    if (K > 0 && take_e == tot_equal) {
+        // every key of the slice at or above T is a candidate: any order
+        // (the list is sorted next), slots handed out per warp
         if (tid == 0) sel[0] = 0;
         __syncthreads();
-        for (int p = tid; p < lim; p += kThreads) {
+        for (int p0 = s0; p0 < s1; p0 += kThreads) {
+            const int p = p0 + tid;
+            const uint32_t key = p < s1 ? order_key(x(p)) : 0u;
+            const bool c = p < s1 && key >= prefix;
+            const unsigned bal = __ballot_sync(0xffffffffu, c);
+            int base = 0;
+            if (lane == 0 && bal) base = atomicAdd(&sel[0], __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (c) own[base + __popc(bal & ((1u << lane) - 1u))] = pack_cand(key, p);
+        }
+    } else if (K > 0) {
+        // only the first take_e keys equal to T, in position order: thread
+        // tid takes the contiguous positions [q0, q1) and finds where its
+        // keys go from two block-wide scans
+        const int per = (s1 - s0 + kThreads - 1) / kThreads;
+        const int q0 = min(s1, s0 + tid * per), q1 = min(s1, q0 + per);
+        int na = 0, ne = 0;
+        for (int p = q0; p < q1; ++p) {
             const uint32_t key = order_key(x(p));
-            if (key > prefix) cand[atomicAdd(&sel[0], 1)] = pack_cand(key, p);
+            na += key > prefix;
+            ne += key == prefix;
         }
-        int taken = 0;
-        for (int base = 0; base < lim && taken < need; base += kThreads) {
-            const int p = base + tid;
-            const bool eq = p < lim && order_key(x(p)) == prefix;
-            const unsigned bal = __ballot_sync(0xffffffffu, eq);
-            if (lane == 0) warp_sums[warp] = __popc(bal);
-            __syncthreads();
-            int before = 0, total = 0;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const int v = warp_sums[w];
-                before += w < warp ? v : 0;
-                total += v;
+        int ta, te;
+        int ia = block_exclusive_scan(na, scan_buf, ta);
+        int ie = block_exclusive_scan(ne, scan_buf, te);
+        for (int p = q0; p < q1; ++p) {
+            const uint32_t key = order_key(x(p));
+            if (key > prefix) own[ia++] = pack_cand(key, p);
+            else if (key == prefix) {
+                if (ie < take_e) own[tot_above + ie] = pack_cand(key, p);
+                ++ie;
             }
-            const int rank = taken + before + __popc(bal & ((1u << lane) - 1u));
-            if (eq && rank < need) cand[n_above + rank] = pack_cand(prefix, p);
-            taken += total;
-            __syncthreads();
         }
     }
-
-    // bitonic sort of K entries (padded with 0, which sorts last) into
-    // descending order
+    // pad to a power of two with 0 (sorts last)
     int P = 1;
-    while (P < K) P <<= 1;
-    for (int i = K + tid; i < P; i += kThreads) cand[i] = 0ull;
+    while (P < m) P <<= 1;
+    for (int i = m + tid; i < P; i += kThreads) own[i] = 0ull;
     __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < P / 2; i += kThreads) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const unsigned long long u = cand[lo], v = cand[hi];
-                if ((u < v) == desc) {
-                    cand[lo] = v;
-                    cand[hi] = u;
+
+    // ---------------------------------------------------------------- 3. sort, rank, place
+    if (P <= kThreads) {
+        // one entry per thread (threads past P hold 0): the same network, the
+        // partner within the warp reached by a shuffle, beyond it through
+        // shared memory
+        unsigned long long v = tid < P ? own[tid] : 0ull;
+        for (int size = 2; size <= kThreads; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                unsigned long long o;
+                if (stride >= 32) {
+                    __syncthreads();
+                    own[tid] = v;
+                    __syncthreads();
+                    o = own[tid ^ stride];
+                } else {
+                    o = __shfl_xor_sync(0xffffffffu, v, stride);
                 }
+                // the lower index of a pair keeps the larger value in a
+                // descending block, the smaller in an ascending one
+                const bool desc = (tid & size) == 0;
+                const bool lower = (tid & stride) == 0;
+                v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
             }
-            __syncthreads();
+        }
+        __syncthreads();
+        if (tid < P) own[tid] = v;
+        __syncthreads();
+    } else {
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P / 2; i += kThreads) {
+                    const int lo = 2 * i - (i & (stride - 1));
+                    const int hi = lo + stride;
+                    const bool desc = (lo & size) == 0;
+                    const unsigned long long u = own[lo], w = own[hi];
+                    if ((u < w) == desc) {
+                        own[lo] = w;
+                        own[hi] = u;
+                    }
+                }
+                __syncthreads();
+            }
         }
     }
-
+    if (tid == 0) {
+        counts[2] = taken_before;
+        counts[3] = m;
+    }
+    __syncthreads();
+    cluster_sync();
+    // every list into `all`, each at its offset (this CTA's own too)
+    if (tid < 2 * kSlices)
+        slice_counts[2 + tid / kSlices][tid % kSlices] =
+            (int)ld_cluster_u32(remote_addr(&counts[2 + tid / kSlices], (uint32_t)(tid % kSlices)));
+    __syncthreads();
+    int offs[kSlices], lens[kSlices];
+#pragma unroll
+    for (int r = 0; r < kSlices; ++r) {
+        offs[r] = slice_counts[2][r];
+        lens[r] = slice_counts[3][r];
+    }
+    // entry j of the concatenated lists (list r holds [offs[r], offs[r] +
+    // lens[r])), eight loads in flight per thread
+    for (int j0 = 0; j0 < K; j0 += 8 * kThreads) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u * kThreads + tid;
+            v[u] = 0ull;
+            if (j < K) {
+                int r = 0;
+#pragma unroll
+                for (int q = 1; q < kSlices; ++q) r += j >= offs[q] ? 1 : 0;
+                v[u] = ld_cluster_u64(remote_addr(own + (j - offs[r]), (uint32_t)r));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u * kThreads + tid;
+            if (j < K) all[j] = v[u];
+        }
+    }
+    __syncthreads();
     int32_t* oi = a.indices + (long long)row * a.indices_stride;
     uint32_t* ov = a.values ? reinterpret_cast<uint32_t*>(a.values) + (long long)row * a.values_stride
                             : nullptr;
-    for (int i = tid; i < a.k; i += kThreads) {
-        if (i < K) {
-            const unsigned long long c = cand[i];
-            oi[i] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
-            if (ov) ov[i] = key_bits((uint32_t)(c >> 32));
-        } else {
+    for (int i = tid; i < m; i += kThreads) {
+        const unsigned long long c = own[i];
+        int rk = i;
+        for (int r = 0; r < kSlices; ++r) {
+            if (r == (int)rank) continue;
+            // entries of list r greater than c (the list is descending)
+            int lo = 0, hi = lens[r];
+            const unsigned long long* L = all + offs[r];
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (L[mid] > c) lo = mid + 1;
+                else hi = mid;
+            }
+            rk += lo;
+        }
+        oi[rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
+        if (ov) ov[rk] = key_bits((uint32_t)(c >> 32));
+    }
+    if (rank == 0) {
+        for (int i = K + tid; i < a.k; i += kThreads) {
             oi[i] = -1;
             if (ov) ov[i] = 0xFF800000u;     // -inf
         }
     }
+    // no CTA leaves while another may still read its shared memory
+    cluster_sync();
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream)
 {
-    // static shared memory of the kernel, plus the largest row copy that fits
-    constexpr int kStatic = 256 * 4 + kTopkMax * 8 + kWarps * 4 + 8;
-    const int cache_bytes = (smem_optin - kStatic - 1024) & ~15;
-    const int cache_elems = cache_bytes > 0 ? cache_bytes / 4 : 0;
+    // dynamic shared memory: the sort buffer (k rounded up to a power of
+    // two, at least kThreads), the lists of all slices (k), and the largest slice copy that fits
+    // under a budget that keeps four CTAs on an SM (larger slices are read
+    // from global memory on every pass)
+    // (at least one entry per thread: the in-register sort goes through it)
+    int sort_cap = kThreads;
+    while (sort_cap < a.k) sort_cap <<= 1;
+    const size_t lists = (size_t)(sort_cap + a.k) * 8;
+    const size_t budget = 54 * 1024;
+    const long long chunk = ((long long)a.max_context + kSlices - 1) / kSlices;
+    long long cache_elems = budget > lists ? (long long)(budget - lists) / 4 : 0;
+    if (cache_elems > chunk) cache_elems = chunk;
+    const size_t smem = lists + (size_t)cache_elems * 4;
+    if (smem + 4 * 1024 > (size_t)smem_optin) return cudaErrorInvalidConfiguration;
     static int configured_device = -1;
-    static int configured_bytes = -1;
+    static size_t configured_bytes = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev || configured_bytes != cache_bytes) {
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 cache_bytes > 0 ? cache_bytes : 0);
+    if (configured_device != dev || configured_bytes < smem) {
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured_device = dev;
-        configured_bytes = cache_bytes;
+        configured_bytes = smem;
     }
-    topk_kernel<<<rows, kThreads, cache_bytes > 0 ? cache_bytes : 0, stream>>>(a, cache_elems);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows * kSlices);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSlices;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel, a, (int)cache_elems, sort_cap);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
