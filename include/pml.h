@@ -219,6 +219,31 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
                              int64_t scores_stride, int max_context, void* stream);
 
 /*
+ * pml_fp8_paged_mqa_logits_wait_test -- test support; the pages have no
+ * counterpart.  The fp32 fp8 logits call with the in-kernel schedule, in which
+ * every CTA's producer leaves its stage number drop_stage (counted from 0
+ * within the CTA) unpublished, and every wait inside the kernel gives up after
+ * wait_limit_us microseconds instead of one second.  The roles waiting on the
+ * missing stage run out of time: the CTA records PML_STATUS_WAIT_TIMEOUT,
+ * raises its abort flag so that its other roles stop waiting, lets the copies
+ * and MMAs it issued complete, frees its tensor memory and returns.  Logits of
+ * the CTAs that stopped are incomplete.  It exists so that the tests can run
+ * the kernel's timeout path on the GPU without a fault or a hang: the call
+ * returns, the status word says what happened, and the device stays usable
+ * for the next call.
+ *
+ * Arguments as pml_fp8_paged_mqa_logits (fp32 out, no schedule_meta, default
+ * CTA count).  Returns PML_ERR_INVALID_ARG for drop_stage < 0 or
+ * wait_limit_us outside 1 .. 1000000, else as pml_fp8_paged_mqa_logits.
+ */
+int pml_fp8_paged_mqa_logits_wait_test(const uint8_t* q, const uint8_t* kv_fused,
+                                       int64_t num_blocks, const float* weights,
+                                       const int32_t* seq_lens, const int32_t* block_table,
+                                       int64_t bt_stride, float* out, int64_t out_stride,
+                                       int max_context, int batch, int next_n, int num_heads,
+                                       int drop_stage, int64_t wait_limit_us, void* stream);
+
+/*
  * pml_fp4_paged_mqa_logits -- the MXFP4 variant ("flashinfer.attn_scores":
  * the math block, its two bullets and the paragraph after them: MXFP4 block
  * scales folded into the dequantised values, one per 32-element group on

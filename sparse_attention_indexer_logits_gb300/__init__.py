@@ -37,7 +37,7 @@ __all__ = [
     "pml_fp8_paged_mqa_logits_ex",
     "pml_indexer_scores_bf16", "pml_indexer_scores_nvfp4", "pml_topk_logits",
     "pml_fp4_paged_mqa_logits",
-    "pml_fp8_paged_mqa_logits_noalloc",
+    "pml_fp8_paged_mqa_logits_noalloc", "pml_fp8_paged_mqa_logits_wait_test",
     "pml_device_status",
     "pml_default_num_ctas", "pml_min_block_table_width", "pml_padded_seq_len", "pml_schedule_meta_elems",
     "fp8_paged_mqa_logits", "indexer_scores", "compute_paged_mqa_logits_schedule",
@@ -100,6 +100,9 @@ def lib() -> ctypes.CDLL:
         L.pml_fp4_paged_mqa_logits.argtypes = [P, P, P, i64, P, P, P, i64, P, i32, P, i64, i32,
                                                i32, i32, i32, P]
         L.pml_fp4_paged_mqa_logits.restype = i32
+        L.pml_fp8_paged_mqa_logits_wait_test.argtypes = [P, P, i64, P, P, P, i64, P, i64, i32, i32,
+                                                         i32, i32, i32, i64, P]
+        L.pml_fp8_paged_mqa_logits_wait_test.restype = i32
         L.pml_fp8_paged_mqa_logits_noalloc.argtypes = [P, P, i64, P, P, P, i64, i32, P, i64, i32,
                                                        i32, i32, i32, P]
         L.pml_fp8_paged_mqa_logits_noalloc.restype = i32
@@ -368,6 +371,31 @@ def pml_fp4_paged_mqa_logits(q: torch.Tensor, q_sf: torch.Tensor, kv_cache: torc
         _ptr(seq_lens), _ptr(block_table), block_table.stride(0), _ptr(schedule_meta), num_ctas,
         _ptr(out), out.stride(0), _OUT_DTYPES[out.dtype], max_context, batch, next_n,
         _stream(stream)), "pml_fp4_paged_mqa_logits")
+    return out
+
+
+def pml_fp8_paged_mqa_logits_wait_test(q: torch.Tensor, kv_fused: torch.Tensor,
+                                       weights: torch.Tensor, seq_lens: torch.Tensor,
+                                       block_table: torch.Tensor, out: torch.Tensor,
+                                       max_context: int, next_n: int, drop_stage: int,
+                                       wait_limit_us: int, stream=None) -> torch.Tensor:
+    """Test support (no counterpart on the pages): the fp32 fp8 logits call in
+    which every CTA's producer leaves its stage ``drop_stage`` unpublished and
+    every in-kernel wait gives up after ``wait_limit_us``, so that the
+    kernel's timeout path runs: PML_STATUS_WAIT_TIMEOUT is set and the call
+    returns with those CTAs' logits incomplete."""
+    for t, nm in ((q, "q"), (kv_fused, "kv_fused"), (weights, "weights"), (seq_lens, "seq_lens")):
+        _cuda(t, nm)
+    _cuda(block_table, "block_table", contiguous=False)
+    _cuda(out, "out", contiguous=False)
+    if out.dtype != torch.float32 or out.stride(-1) != 1 or block_table.stride(-1) != 1:
+        raise ValueError("out must be float32; out and block_table need unit last stride")
+    batch = seq_lens.numel()
+    _check(lib().pml_fp8_paged_mqa_logits_wait_test(
+        _ptr(q), _ptr(kv_fused), kv_fused.numel() // 8448, _ptr(weights), _ptr(seq_lens),
+        _ptr(block_table), block_table.stride(0), _ptr(out), out.stride(0), max_context, batch,
+        next_n, q.shape[1], drop_stage, wait_limit_us, _stream(stream)),
+        "pml_fp8_paged_mqa_logits_wait_test")
     return out
 
 

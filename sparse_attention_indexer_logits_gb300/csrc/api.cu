@@ -168,12 +168,17 @@ int pml_fp8_paged_mqa_logits(const uint8_t* q, const uint8_t* kv_fused, int64_t 
                                        stream);
 }
 
-int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
-                                const float* weights, const int32_t* seq_lens,
-                                const int32_t* block_table, int64_t bt_stride,
-                                const int32_t* schedule_meta, int num_ctas, void* out,
-                                int64_t out_stride, int output_dtype, int max_context, int batch,
-                                int next_n, int num_heads, void* stream)
+}  // extern "C"
+
+namespace {
+
+// The fp8 logits call with the longest wait of any role and, for tests, a
+// stage the producer leaves unpublished (-1: none).
+int fp8_logits_call(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
+                    const float* weights, const int32_t* seq_lens, const int32_t* block_table,
+                    int64_t bt_stride, const int32_t* schedule_meta, int num_ctas, void* out,
+                    int64_t out_stride, int output_dtype, int max_context, int batch, int next_n,
+                    int num_heads, void* stream, unsigned long long wait_limit_ns, int drop_stage)
 {
     if (batch < 0 || num_ctas < 0) return PML_ERR_INVALID_ARG;
     if (output_dtype != PML_DTYPE_FLOAT32 && output_dtype != PML_DTYPE_BFLOAT16)
@@ -214,6 +219,8 @@ int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64
     a.batch = batch;
     a.next_n = next_n;
     a.max_context = max_context;
+    a.wait_limit_ns = wait_limit_ns;
+    a.drop_stage = drop_stage;
     const int n_pad = (next_n * num_heads + 15) / 16 * 16;
     a.q_box_rows = (int)(rows_total < n_pad ? rows_total : n_pad);
     const size_t fixed = fp8_smem_bytes(next_n, num_heads, 0);
@@ -240,6 +247,36 @@ int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64
     }
     e = launch_fp8_logits(num_heads, kmap, qmap, a, num_ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pml_fp8_paged_mqa_logits_ex(const uint8_t* q, const uint8_t* kv_fused, int64_t num_blocks,
+                                const float* weights, const int32_t* seq_lens,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* schedule_meta, int num_ctas, void* out,
+                                int64_t out_stride, int output_dtype, int max_context, int batch,
+                                int next_n, int num_heads, void* stream)
+{
+    return fp8_logits_call(q, kv_fused, num_blocks, weights, seq_lens, block_table, bt_stride,
+                           schedule_meta, num_ctas, out, out_stride, output_dtype, max_context,
+                           batch, next_n, num_heads, stream, kWaitLimitNs, -1);
+}
+
+int pml_fp8_paged_mqa_logits_wait_test(const uint8_t* q, const uint8_t* kv_fused,
+                                       int64_t num_blocks, const float* weights,
+                                       const int32_t* seq_lens, const int32_t* block_table,
+                                       int64_t bt_stride, float* out, int64_t out_stride,
+                                       int max_context, int batch, int next_n, int num_heads,
+                                       int drop_stage, int64_t wait_limit_us, void* stream)
+{
+    if (drop_stage < 0 || wait_limit_us < 1 || wait_limit_us > 1000000) return PML_ERR_INVALID_ARG;
+    return fp8_logits_call(q, kv_fused, num_blocks, weights, seq_lens, block_table, bt_stride,
+                           nullptr, 0, out, out_stride, PML_DTYPE_FLOAT32, max_context, batch,
+                           next_n, num_heads, stream,
+                           (unsigned long long)wait_limit_us * 1000ull, drop_stage);
 }
 
 int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv_cache,

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                             if (lane == ol) {
                                 const int slot = qidx & 1;
                                 ok = mbar_wait<kCallWait>(qempty_bar0 + 8u * slot,
-                                                          ((qidx >> 1) & 1) ^ 1, abort_flag, a.status);
+                                                          ((qidx >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_limit_ns);
                                 if (ok) {
                                     const uint32_t qfb = qfull_bar0 + 8u * slot;
                                     mbar_arrive_expect_tx(qfb,
@@ -400,28 +400,31 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                         }
                     }
                     if (!ok) break;
-                    if (lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+                    if (lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status, a.wait_limit_ns);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     // publish the stage: each owner lane its sub-tile, lane 0 the rest
+                    // (not at all for the stage a test asks to leave out: the roles
+                    // waiting on it then run out of time and the CTA aborts)
+                    const bool publish = issued != a.drop_stage;
                     StageDesc& sd = descs[s];
-                    if (own) {
+                    if (own && publish) {
                         const int meta = win.cnt | (win.first ? kMetaFirst : 0) |
                                          (win.last ? kMetaLast : 0) | ((qidx & 1) << kMetaSlotShift);
                         *reinterpret_cast<int4*>(&sd.sub[i]) = make_int4(win.b, win.j, win.len, meta);
                     }
-                    if (lane == 0) {
+                    if (lane == 0 && publish) {
                         for (int k = win.n - o0; k < KT; ++k)
                             *reinterpret_cast<int4*>(&sd.sub[k]) = make_int4(0, 0, 0, 0);
                     }
                     const unsigned m0 = __ballot_sync(0xffffffffu, own && win.ld0);
                     const unsigned m1 = __ballot_sync(0xffffffffu, own && win.ld1);
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0 && publish)
                         mbar_arrive_expect_tx(full_bar0 + 8u * s,
                                               (uint32_t)(__popc(m0) + __popc(m1)) * kFp8BlockBytes);
                     __syncwarp();
-                    if (own) {
+                    if (own && publish) {
                         const uint32_t kdst = k_base + s * kStageKeyBytes + (uint32_t)i * kSubKeyBytes;
                         const uint32_t sdst = s_base + s * kStageScaleBytes + (uint32_t)i * kSubScaleBytes;
                         if (win.ld0) load_block(kdst, sdst, win.phys0);
@@ -440,24 +443,32 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 if (!have_nxt) nxt = make_window<KT>(a, win.nb, win.nj, sb, sj, eb, ej, lane);
                 win = nxt;
             }
+            bool end_written = false;
             if (ok && lane == 0) {
                 // end marker for the MMA and epilogue warps, in the stage after the last one
-                ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status);
+                ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status, a.wait_limit_ns);
                 if (ok) {
                     *reinterpret_cast<int4*>(&descs[s].sub[0]) = make_int4(0, 0, 0, kStageEnd);
                     mbar_arrive(full_bar0 + 8u * s);
+                    end_written = true;
                 }
             }
-            if (!ok && lane == 0) {
-                // drain: let every copy this warp issued land before the CTA exits
+            if (lane == 0) {
+                // drain: every copy this warp issued lands before the CTA exits,
+                // also when the consumers stopped early (on the normal path these
+                // phases have completed already).  The end marker's stage is left
+                // out: its barrier has moved on, and the copies of its earlier use
+                // were consumed before the marker could take the stage.
+                const int depth = end_written ? S - 1 : S;
                 uint32_t ds = s, dph = ph;
-                for (int t = 0; t < issued && t < S; ++t) {
+                for (int t = 0; t < issued && t < depth; ++t) {
                     if (ds == 0) { ds = S; dph ^= 1; }
                     --ds;
-                    mbar_wait_drain<kCallWait>(full_bar0 + 8u * ds, dph);
+                    if (issued - 1 - t != a.drop_stage)   // that one holds no copies
+                        mbar_wait_drain<kCallWait>(full_bar0 + 8u * ds, dph, a.wait_limit_ns);
                 }
                 for (int qc = (q_issued > 2 ? q_issued - 2 : 0); qc < q_issued; ++qc)
-                    mbar_wait_drain<kCallWait>(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1);
+                    mbar_wait_drain<kCallWait>(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1, a.wait_limit_ns);
             }
         } else if (warp == kMmaWarp || warp == kMmaWarp2) {
             // ------------------------------------------------------------ MMA issuers
@@ -474,12 +485,12 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 int qcount = 0, done = 0;
                 bool ok = true;
                 while (true) {
-                    ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
+                    ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status, a.wait_limit_ns);
                     if (!ok) break;
                     const int4 x0 = load_sub(descs + s, 0);
                     const int4 x1 = KT == 2 ? load_sub(descs + s, 1) : make_int4(0, 0, 0, 0);
                     if (x0.w & kStageEnd) break;
-                    ok = mbar_wait<kCallWait>(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status);
+                    ok = mbar_wait<kCallWait>(tempty_bar0 + 8u * acc, aph ^ 1, abort_flag, a.status, a.wait_limit_ns);
                     if (!ok) break;
                     // q / weights of every request that starts in this stage, in order
 #pragma unroll
@@ -487,7 +498,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                         const int meta = i == 0 ? x0.w : x1.w;
                         if (ok && (meta & kMetaFirst)) {
                             ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * meta_slot(meta),
-                                                      (qcount >> 1) & 1, abort_flag, a.status);
+                                                      (qcount >> 1) & 1, abort_flag, a.status, a.wait_limit_ns);
                             ++qcount;
                         }
                     }
@@ -519,7 +530,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 if (done > 0) {
                     // every MMA this warp issued has completed before TMEM is
                     // released: the phase of its last commit completes only then
-                    mbar_wait_drain<kCallWait>(tfull_bar0 + 8u * last_acc, last_ph);
+                    mbar_wait_drain<kCallWait>(tfull_bar0 + 8u * last_acc, last_ph, a.wait_limit_ns);
                 }
             }
         }
@@ -542,7 +553,7 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
         int qcount = 0;
         bool ok = true;
         while (true) {
-            ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status);
+            ok = mbar_wait<kCallWait>(full_bar0 + 8u * s, ph, abort_flag, a.status, a.wait_limit_ns);
             if (!ok) break;
             const int4 x0 = load_sub(descs + s, 0);
             const int4 x1 = KT == 2 ? load_sub(descs + s, 1) : make_int4(0, 0, 0, 0);
@@ -554,12 +565,12 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 const int meta = i == 0 ? x0.w : x1.w;
                 if (ok && (meta & kMetaFirst)) {
                     ok = mbar_wait<kCallWait>(qfull_bar0 + 8u * meta_slot(meta), (qcount >> 1) & 1,
-                                              abort_flag, a.status);
+                                              abort_flag, a.status, a.wait_limit_ns);
                     ++qcount;
                 }
             }
             if (!ok) break;
-            ok = mbar_wait<kCallWait>(tfull_bar0 + 8u * acc, aph, abort_flag, a.status);
+            ok = mbar_wait<kCallWait>(tfull_bar0 + 8u * acc, aph, abort_flag, a.status, a.wait_limit_ns);
             if (!ok) break;
             tc_fence_after();
             // The MMAs of this stage are complete, so its key buffers are no

@@ -25,6 +25,9 @@ struct Fp8Args {
     int stages;       // depth of the K-page ring
     int q_box_rows;   // rows one Q load brings (<= MMA N)
     int out_bf16;     // 1: logits stored as bf16 (round to nearest even)
+    unsigned long long wait_limit_ns;   // longest wait of any role (kWaitLimitNs normally)
+    int drop_stage;   // test support: the stage (count within each CTA) the producer
+                      // leaves unpublished, so the roles waiting on it run out of time; -1: none
 };
 
 struct Bf16Args {

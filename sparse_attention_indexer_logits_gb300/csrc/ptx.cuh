@@ -117,19 +117,19 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// Slow path of mbar_wait: spin for at most kWaitLimitNs.  Gives up early
+// Slow path of mbar_wait: spin for at most limit_ns.  Gives up early
 // (returning false) once *abort is set by another role of the CTA.  On
 // timeout, records kStatusWaitTimeout in *status, raises *abort and returns
 // false.  Never spins forever.
 __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status)
+                                          unsigned int* status, uint64_t limit_ns = kWaitLimitNs)
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
         if ((it & 31u) == 0) {
             if (abort != nullptr && *abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 if (status) atomicOr(status, kStatusWaitTimeout);
                 if (abort) *abort = 1;
                 return false;
@@ -140,9 +140,10 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatil
 
 // The slow path out of line, which keeps the loops around the waits short.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                                   volatile int* abort, unsigned int* status)
+                                                   volatile int* abort, unsigned int* status,
+                                                   uint64_t limit_ns)
 {
-    return mbar_spin(bar, parity, abort, status);
+    return mbar_spin(bar, parity, abort, status, limit_ns);
 }
 
 // Wait for the phase with the given parity to complete (bounded, see above).
@@ -150,19 +151,20 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // registers between warpgroups (setmaxnreg) must contain no calls.
 template <bool kCall = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status)
+                                          unsigned int* status, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    if constexpr (kCall) return mbar_wait_slow(bar, parity, abort, status);
-    else return mbar_spin(bar, parity, abort, status);
+    if constexpr (kCall) return mbar_wait_slow(bar, parity, abort, status, limit_ns);
+    else return mbar_spin(bar, parity, abort, status, limit_ns);
 }
 
 // Same, ignoring the abort flag: used while draining copies already in flight
 // before the CTA exits.
 template <bool kCall = true>
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                uint64_t limit_ns = kWaitLimitNs)
 {
-    return mbar_wait<kCall>(bar, parity, nullptr, nullptr);
+    return mbar_wait<kCall>(bar, parity, nullptr, nullptr, limit_ns);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -151,6 +151,14 @@ def _fp4(L, **over):
                                       a["out_stride"], a["dt"], a["mc"], a["batch"], a["n"], None)
 
 
+def test_wait_test_argument_checks(L):
+    def call(drop, limit):
+        return L.pml_fp8_paged_mqa_logits_wait_test(P, P, 4, P, P, P, 4, P, 256, 256, 2, 1, 64,
+                                                    drop, limit, None)
+    assert call(-1, 1000) == 1                        # a stage to leave out is required
+    assert call(0, 0) == 1 and call(0, 1000001) == 1  # limit 1 us .. 1 s
+
+
 def test_fp4_argument_checks(L):
     assert _fp4(L, batch=0) == 0
     assert _fp4(L, dt=7) == 2                         # output type
