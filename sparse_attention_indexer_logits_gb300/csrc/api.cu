@@ -18,9 +18,7 @@ using namespace pml;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxFp8Stages = 12;
 constexpr int kMaxBf16Stages = 8;
-constexpr int kMaxNvfp4Stages = 32;
 constexpr int kMaxMxfp4Stages = 24;
-constexpr int kNvfp4Tiles = 6;   // key tiles in tensor memory: three per side
 
 thread_local int g_last_cuda_error = 0;
 
@@ -89,19 +87,26 @@ cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000& fn)
     return cudaSuccess;
 }
 
-// Tiled map with the 128-byte swizzle: dims/strides innermost first, strides
-// in bytes for dimensions 1.. .
-cudaError_t encode_sw128(CUtensorMap& map, CUtensorMapDataType dtype, int rank, const void* base,
-                         const uint64_t* dims, const uint64_t* strides, const uint32_t* box)
+// Tiled map: dims/strides innermost first, strides in bytes for dimensions 1.. .
+cudaError_t encode_tiled(CUtensorMap& map, CUtensorMapDataType dtype, int rank, const void* base,
+                         const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                         CUtensorMapSwizzle swizzle)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn;
     cudaError_t e = encoder(fn);
     if (e != cudaSuccess) return e;
     const uint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(&map, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The same with the 128-byte swizzle.
+cudaError_t encode_sw128(CUtensorMap& map, CUtensorMapDataType dtype, int rank, const void* base,
+                         const uint64_t* dims, const uint64_t* strides, const uint32_t* box)
+{
+    return encode_tiled(map, dtype, rank, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -422,20 +427,25 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
     a.groups = groups;
     a.group_size = G;
     a.max_context = max_context;
-    a.fused = (key_scales == key_cache + (int64_t)kBlockKeys * kHeadDim / 2 &&
-               scale_page_stride_bytes == page_stride_bytes)
-                  ? 1
-                  : 0;
-    // as many staging slots (9 KB) as fit; both they and the key tiles
-    // split evenly between the kernel's two sides
-    a.tiles = kNvfp4Tiles;
-    const size_t fixed = nvfp4_smem_bytes(0, a.tiles);
-    const size_t per_stage = nvfp4_smem_bytes(1, a.tiles) - fixed;
+    a.scales16 = (aligned(key_scales, 16) && scale_page_stride_bytes % 16 == 0) ? 1 : 0;
+    // as many four-page stages (18 KB) as fit
+    const size_t fixed = nvfp4_smem_bytes(0);
+    const size_t per_stage = nvfp4_smem_bytes(1) - fixed;
     if ((size_t)dev.smem_optin < fixed + 2 * per_stage) return PML_ERR_UNSUPPORTED;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
-    if (stages > kMaxNvfp4Stages) stages = kMaxNvfp4Stages;
-    a.stages = stages & ~1;
-    e = launch_nvfp4_scores(a, dev.sm_count, static_cast<cudaStream_t>(stream));
+    a.stages = stages > kMaxNvfp4Stages ? kMaxNvfp4Stages : stages;
+    // the codes of page P: 64 rows of 64 bytes at P * page_stride, landing
+    // with the 64-byte swizzle the MMA reads
+    CUtensorMap kmap;
+    {
+        const uint64_t dims[3] = {(uint64_t)kHeadDim / 2, (uint64_t)kBlockKeys, (uint64_t)num_pages};
+        const uint64_t strides[2] = {(uint64_t)kHeadDim / 2, (uint64_t)page_stride_bytes};
+        const uint32_t box[3] = {(uint32_t)kHeadDim / 2, (uint32_t)kBlockKeys, 1};
+        e = encode_tiled(kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, key_cache, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_64B);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_nvfp4_scores(kmap, a, dev.sm_count, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 

@@ -47,6 +47,9 @@ struct Bf16Args {
     int q_box_rows;
 };
 
+// Stages of the NVFP4 kernel: each has 16 tensor-memory columns of key scales.
+constexpr int kMaxNvfp4Stages = 20;
+
 struct Nvfp4Args {
     const uint8_t* query;          // [rows][64] packed E2M1
     const uint8_t* query_scales;   // [rows][8] E4M3
@@ -66,10 +69,9 @@ struct Nvfp4Args {
     int groups;
     int group_size;
     int max_context;
-    int stages;      // staging slots (packed pages and scales of one tile)
-    int tiles;       // f16 tiles the MMA reads
-    int fused;       // 1: a page's scales follow its codes (key_scales == key_cache + 4096,
-                     // one page stride), so one bulk copy brings both
+    int stages;      // stages of one four-page tile (codes, then scales), <= kMaxNvfp4Stages
+    int scales16;    // 1: key_scales and its page stride are 16-byte aligned (one
+                     // 16-byte cp.async per lane and page), else two of 8 bytes
 };
 
 struct Mxfp4Args {
@@ -112,14 +114,15 @@ struct TopkArgs {
 // Bytes of dynamic shared memory the fp8 kernel needs for `stages`.
 size_t fp8_smem_bytes(int next_n, int num_heads, int stages);
 size_t bf16_smem_bytes(int stages);
-size_t nvfp4_smem_bytes(int stages, int tiles);
+size_t nvfp4_smem_bytes(int stages);
 size_t mxfp4_smem_bytes(int slots_per_pass, int stages);
 
 cudaError_t launch_fp8_logits(int num_heads, const CUtensorMap& kmap, const CUtensorMap& qmap,
                               const Fp8Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
                                const Bf16Args& a, int num_ctas, cudaStream_t stream);
-cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_nvfp4_scores(const CUtensorMap& kmap, const Nvfp4Args& a, int num_ctas,
+                                cudaStream_t stream);
 // The MXFP4 logits: one launch per pass of at most two query slots.
 cudaError_t launch_mxfp4_logits(const Mxfp4Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream);

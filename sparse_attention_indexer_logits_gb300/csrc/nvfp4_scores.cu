@@ -9,33 +9,46 @@
 // of 8; a score is the plain dot product of the dequantised query row and
 // key.)
 //
-// A dequantising stage in front of the tensor cores.  A value is an E2M1 code
-// (at most 2 significant bits) times an E4M3 scale (at most 4), so it has at
-// most 6 significant bits and |v| <= 6 * 448 = 2688: exact in f16.  Each tile
-// of two 64-key pages therefore becomes an f16 operand with no rounding, and
-// tcgen05.mma kind::f16 accumulates the exact f16 products in fp32.  The key
-// tile (A) is written to tensor memory, not shared memory: that halves the
-// shared-memory traffic of a tile, which would otherwise bound the kernel.
+// The tensor cores take the format as stored.  tcgen05.mma kind::mxf4nvf4
+// with 16-element scale blocks multiplies E2M1 codes of A (128 keys, K-major)
+// and B (the group's rows padded to N = 16), scales each block's partial sum
+// by the two E4M3 scales it reads from tensor memory and accumulates in fp32:
+// no dequantising pass, two MMAs (K = 64) per 128 keys.  The MMA reads a scale
+// byte without its sign (and 0x7f / 0xff as NaN, like the format), so a
+// negative scale is applied by flipping the sign bits of its block's sixteen
+// codes in shared memory (bit 3 of each nibble) before the MMA reads them.
 //
-//   (every role comes twice, one copy for each side: the even tiles and the
-//   odd tiles)
-//   warps 0,10 producers: per tile one bulk copy per page -- 4608 bytes of
-//              codes and scales when the scales follow the codes, else the
-//              4 KB of codes and 8-byte cp.async copies of the 512 scale bytes
-//              (their pages need only 8-byte alignment) -- completing on the
-//              staging slot's `full` barrier, plus a 8-byte record of the
-//              tile's group.  Staging slots (9 KB) fill most of the shared
-//              memory, so many copies are in flight.
-//   warps 1,11 MMA issue: 8 tcgen05.mma (K = 16) per tile, A from tensor
-//              memory, B the group's rows (padded to N = 16) in shared memory,
-//              one commit, into one of eight TMEM accumulators (16 columns
-//              each; a side uses the four of its parity).
-//   warps 2-5, 16-19 epilogues: one key per thread, up to 8 scores per key.
-//   warps 6-9, 12-15 dequantisation: a thread expands one key row --
-//              cvt.rn.f16x2.e2m1x2 per byte and one f16x2 multiply by the
-//              group's scale -- into its TMEM lane (tcgen05.st, 64 columns);
-//              per group of query rows, the rows into one of the side's two
-//              Q slots (shared memory, 128-byte-swizzled K-major).
+// Scale layout in tensor memory (one 32-bit column holds the four scales of a
+// row's K = 64 half, byte b for elements 16b..16b+15):
+//   A: row m is read from lane m, column sfa + m / 32;
+//   B: row n, for the output rows of lane quadrant q, from lane 32 q + n,
+//      column sfb + n / 32 -- every quadrant holds its own copy.
+// Writing each lane's word to all four columns sfa..sfa+3 (and its second
+// K-half's word to sfa+4..sfa+7) satisfies both with one tcgen05.st.
+//
+// A tile is four 64-key pages (two MMA halves of M = 128): the codes arrive by
+// TMA with the 64-byte swizzle (a row of 64 bytes is one swizzle span), so the
+// two pages of a half are the K-major operand as they land; the scales by
+// cp.async into the stage's scale area.
+//
+//   warps 0,2,3 producers, tile i to warp i % 3: per tile the block-table
+//               entries (a 64-entry window in two registers per lane), a TMA
+//               per page for the codes and one or two cp.async per lane and
+//               page for the scales, all completing on the stage's `full`
+//               barrier, and a record of the tile's group; an end mark after
+//               the last tile.  One warp's round per tile (~1.9k cycles,
+//               mostly issue latency) is twice a tile's share of HBM time, so
+//               three take turns.
+//   warp 1      MMA issue: per tile 2 x 2 MMAs into one of four accumulators
+//               (two 16-column halves each); commits free the accumulator's
+//               readers, the stage and, after a group's last tile, its Q slot.
+//   warps 4-7   scales: per tile each thread writes the scale words of keys
+//               (row, 128 + row) to the stage's columns, fixing signs; on a
+//               group's first tile, the query rows into a Q slot (shared
+//               memory, sign-fixed, swizzled) and their scales into the slot's
+//               columns.
+//   warps 8-15  two epilogue warpgroups, even and odd tiles: two keys per
+//               thread, up to 8 scores per key.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -47,104 +60,147 @@ namespace pml {
 
 namespace {
 
-constexpr int kN = 16;                                   // MMA N: group rows padded
-constexpr int kPackedRow = kHeadDim / 2;                 // 64 bytes of codes per row
-constexpr int kScalesPerRow = kHeadDim / 16;             // 8
-constexpr int kPackedPage = kBlockKeys * kPackedRow;     // 4096
-constexpr int kScalePage = kBlockKeys * kScalesPerRow;   // 512
-constexpr int kStagePage = kPackedPage + kScalePage;     // 4608: a staged page, codes then scales
-constexpr int kQHalfBytes = kN * 128;                    // 2 KB
-constexpr int kQSlotBytes = 2 * kQHalfBytes;             // 4 KB
-// Every role comes twice, one copy for each side of the tile sequence (side
-// p = tile index & 1): one role's per-tile chain (waits, lookups, copy
-// issues, conversions, TMEM loads) is longer than a tile's share of HBM time.
-// Each side has its own half of the staging slots, key tiles, accumulators
-// and Q slots, so every barrier has one side's roles on it, in tile order.
-constexpr int kProducerWarp = 0;      // and kProducerWarp2
-constexpr int kMmaWarp = 1;           // and kMmaWarp2; warp 1 also allocates TMEM
-constexpr int kFirstEpiWarp = 2;      // warps 2-5, and 16-19
-constexpr int kFirstDeqWarp = 6;      // warps 6-9, and 12-15
-constexpr int kProducerWarp2 = 10;
-constexpr int kMmaWarp2 = 11;
-constexpr int kFirstDeqWarp2 = 12;
-constexpr int kFirstEpiWarp2 = 16;
-constexpr int kThreads = 640;
-constexpr int kRecFirst = 1;
-// Tensor memory: eight accumulators of N = 16 columns (a side uses the four of
-// its parity), then the f16 key tiles, 64 columns each (128 values of a key
-// row, two per column), `tiles` of them.
-constexpr int kAcc = 8;
-constexpr uint32_t kAccCols = kAcc * kN;                 // 128
-constexpr uint32_t kTileCols = kHeadDim / 2;             // 64
+constexpr int kN = 16;                                     // MMA N: group rows padded
+constexpr int kRowBytes = kHeadDim / 2;                    // 64 bytes of codes per row
+constexpr int kRowScales = kHeadDim / 16;                  // 8
+constexpr int kPageCodes = kBlockKeys * kRowBytes;         // 4096
+constexpr int kPageScales = kBlockKeys * kRowScales;       // 512
+constexpr int kTileBlocks = 4;                             // pages per tile
+constexpr int kHalfCodes = 2 * kPageCodes;                 // one M = 128 operand
+constexpr int kStageCodes = kTileBlocks * kPageCodes;      // 16 KB
+constexpr int kStageBytes = kStageCodes + kTileBlocks * kPageScales;   // 18 KB
+constexpr int kQSlotBytes = kN * kRowBytes;                // 1 KB
+constexpr int kAcc = 4;
+constexpr uint32_t kAccCols = 2 * kN;                      // both halves of a tile
+constexpr uint32_t kSfaCol0 = kAcc * kAccCols;             // 16 columns per stage
+constexpr uint32_t kSfbCol0 = kSfaCol0 + 16u * kMaxNvfp4Stages;   // 8 columns per Q slot
 constexpr uint32_t kTmemCols = 512;
-constexpr int kMaxTiles = (int)((kTmemCols - kAccCols) / kTileCols);   // 6
+static_assert(kSfbCol0 + 16 <= kTmemCols, "scale columns beyond the allocation");
+constexpr int kProducers = 3;       // warps 0, 2, 3: tile i is producer i % 3's
+constexpr int kMmaWarp = 1;
+constexpr int kScaleWarp0 = 4;      // a whole warpgroup: warp w writes lane quadrant w % 4
+constexpr int kEpiWarp0 = 8;        // warps 8-11 even tiles, 12-15 odd tiles
+constexpr int kThreads = 512;
+constexpr int kRecFirst = 1;
+constexpr uint32_t kSignBits = 0x80808080u;   // the sign bits of four E4M3 scales
+constexpr uint32_t kCodeSigns = 0x88888888u;  // the sign bits of eight E2M1 codes
 
-// Shared memory: `stages` staging slots of one tile's two pages (codes then
-// scales, as HBM delivers them; deep, so that many copies are in flight), half
-// of them per side, and two Q slots per side.  The f16 key tiles live in
-// tensor memory (half of `tiles` per side), freed by the MMA's commit.
+// Shared memory: `stages` stages of one tile (four pages of codes, then their
+// scales), two Q slots, an 8-byte record per stage, barriers.
 struct Nvfp4Layout {
     uint32_t stage, q, rec, bar, misc, total;
 };
 
-__host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages, int tiles)
+__host__ __device__ inline Nvfp4Layout nvfp4_layout(int stages)
 {
     Nvfp4Layout L;
-    L.stage = 0;                                               // slot s, page p: 2s + p
-    L.q = L.stage + (uint32_t)stages * 2 * kStagePage;
-    L.rec = L.q + 4 * kQSlotBytes;                             // per staging slot
+    L.stage = 0;
+    L.q = L.stage + (uint32_t)stages * kStageBytes;
+    L.rec = L.q + 2 * kQSlotBytes;
     L.bar = L.rec + (uint32_t)stages * 8;
-    L.misc = L.bar + (uint32_t)(2 * stages + 2 * tiles + 24) * 8;
+    L.misc = L.bar + (uint32_t)(3 * stages + 2 * kAcc + 4) * 8;
     L.total = L.misc + 64;
     return L;
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
-// K-major region whose rows are 128 bytes (8-row atoms of 1 KB).
-__device__ __forceinline__ uint32_t sw128(int r, int c)
+// Shared-memory matrix descriptor for a K-major operand with the 64-byte
+// swizzle: rows of 64 bytes, groups of 8 rows 512 bytes apart; the base is
+// 512-byte aligned and K advances by adding bytes/16 to the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr)
 {
-    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);       // start address
+    d |= static_cast<uint64_t>(1u) << 16;                     // leading byte offset (unused)
+    d |= static_cast<uint64_t>(512u >> 4) << 32;              // stride byte offset
+    d |= static_cast<uint64_t>(1u) << 46;                     // descriptor version
+    d |= static_cast<uint64_t>(4u) << 61;                     // 64-byte swizzle
+    return d;
 }
 
-// Dequantise the 16 values of group g (8 packed bytes w0, w1) with scale code
-// sc into chunks 2(g%4), 2(g%4)+1 of row `row` of K-half g/4.
-__device__ __forceinline__ void dequant_group(uint32_t w0, uint32_t w1, uint32_t sc, int g,
-                                              uint32_t half0, uint32_t half1, int row)
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1), K-major,
+// E4M3 scales (scale format 0), scale-data ids 0, dense.
+__host__ __device__ constexpr uint32_t nvfp4_idesc(uint32_t M, uint32_t N)
 {
-    const uint32_t s2 = e4m3_to_f16x2_dup(sc);
-    uint32_t lo[4], hi[4], h[8];
-    e2m1x8_to_f16x2x4(w0, lo);
-    e2m1x8_to_f16x2x4(w1, hi);
+    return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D (+)= (A * B^T) with 16-element scale blocks, K = 64.
+__device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Columns c..c+3 of this thread's lane := lo, c+4..c+7 := hi (warp-uniform c).
+__device__ __forceinline__ void tmem_st_scales(uint32_t taddr, uint32_t lo, uint32_t hi)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%1,%1,%1,%2,%2,%2,%2};" ::"r"(taddr),
+        "r"(lo), "r"(hi)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v2_u32(uint32_t addr, uint32_t x, uint32_t y)
+{
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+
+// Byte offset of 16-byte chunk c (0..3) of row r in a region written with the
+// 64-byte swizzle (512-byte aligned base).
+__device__ __forceinline__ uint32_t sw64(int r, int c)
+{
+    return (uint32_t)(r * kRowBytes + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// The scale of block j (0..7) of a row's scale words is negative.
+__device__ __forceinline__ bool scale_negative(uint2 sc, int j)
+{
+    const uint32_t w = j < 4 ? sc.x : sc.y;
+    return (w >> (8 * (j & 3) + 7)) & 1u;
+}
+
+// Flip the code signs of every block of key row `kk` of a landed page whose
+// scale is negative (rare: only then does a thread touch the codes).
+__device__ __forceinline__ void fix_key_signs(uint32_t page, int kk, uint2 sc)
+{
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        h[b] = mul_f16x2(lo[b], s2);
-        h[4 + b] = mul_f16x2(hi[b], s2);
+    for (int j = 0; j < 8; ++j) {
+        if (!scale_negative(sc, j)) continue;
+        const uint32_t addr = page + sw64(kk, j >> 1) + 8u * (j & 1);
+        const uint2 v = ld_shared_v2_u32(addr);
+        st_shared_v2_u32(addr, v.x ^ kCodeSigns, v.y ^ kCodeSigns);
     }
-    const uint32_t base = (g < 4) ? half0 : half1;
-    const int c = (g % 4) * 2;
-    st_shared_v4(base + sw128(row, c), h[0], h[1], h[2], h[3]);
-    st_shared_v4(base + sw128(row, c + 1), h[4], h[5], h[6], h[7]);
 }
 
-// Dequantise one 128-value row: 64 packed bytes at `packed` (four 16-byte
-// chunks, two groups each) and 8 scale codes -> f16 in the swizzled layout.
-// The chunks are read starting at chunk `rot`, so that the rows a warp reads
-// together (64 bytes apart) fall in distinct banks when rot = (row / 2) % 4.
-__device__ __forceinline__ void dequant_row(const uint4* packed, uint2 scales, uint32_t half0,
-                                            uint32_t half1, int row, int rot)
+// Blocks in the walk's current tile: up to four, within one group and range.
+__device__ __forceinline__ int tile_blocks(const Walk& w)
 {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int c = (k + rot) & 3;
-        const uint4 v = packed[c];
-        const uint32_t sw = c < 2 ? scales.x : scales.y;
-        dequant_group(v.x, v.y, (sw >> (16 * (c & 1))) & 0xFF, 2 * c, half0, half1, row);
-        dequant_group(v.z, v.w, (sw >> (16 * (c & 1) + 8)) & 0xFF, 2 * c + 1, half0, half1, row);
-    }
+    const int lim = (w.b == w.eb) ? w.ej : w.nbb;
+    return min(lim - w.j, kTileBlocks);
 }
 
-// Position in a ring of n slots and the parity of its current pass, advanced
-// one step at a time (no division by the runtime ring size in the loops).
+// Position in a ring of n slots and the parity of its current pass.
 struct RingPos {
     int idx = 0;
     uint32_t phase = 0;
@@ -157,65 +213,40 @@ struct RingPos {
     }
 };
 
-// Dequantise one 16-byte chunk (32 codes: two groups of 16 with scale codes
-// sa, sb) into 16 f16x2 words, byte i -> word i.
-__device__ __forceinline__ void dequant_chunk(uint4 v, uint32_t sa, uint32_t sb,
-                                              uint32_t (&out)[16])
-{
-    const uint32_t s_a = e4m3_to_f16x2_dup(sa);
-    const uint32_t s_b = e4m3_to_f16x2_dup(sb);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t h[4];
-        e2m1x8_to_f16x2x4(w[q], h);
-        const uint32_t s2 = q < 2 ? s_a : s_b;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) out[4 * q + b] = mul_f16x2(h[b], s2);
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Args a)
+__global__ void __launch_bounds__(kThreads, 1)
+    nvfp4_scores_kernel(const __grid_constant__ CUtensorMap kmap, const Nvfp4Args a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int S = a.stages;     // staging slots
-    const int T = a.tiles;      // f16 tiles
+    const int S = a.stages;
     const int G = a.group_size;
-    const Nvfp4Layout L = nvfp4_layout(S, T);
+    const Nvfp4Layout L = nvfp4_layout(S);
 
     const uint32_t base = smem_addr(smem);
     const uint32_t stage_base = base + L.stage;
-    // per staging slot, written by the producer before the slot's `full`
-    // arrival: {group b, kRecFirst if the side's first tile of b}, or {-1, 0}
-    // after the side's last tile
-    const uint32_t rec_base = base + L.rec;
     const uint32_t q_base = base + L.q;
+    // per stage, written by the producer before the stage's `full` arrival:
+    // {group, kRecFirst on the group's first tile in this CTA}, or {-1, 0}
+    // after the last tile
+    const uint32_t rec_base = base + L.rec;
     const uint32_t bar = base + L.bar;
-    auto full_bar = [&](int s) { return bar + 8u * s; };                  // staging landed
-    auto sfree_bar = [&](int s) { return bar + 8u * (S + s); };           // staging read
-    auto deq_bar = [&](int t) { return bar + 8u * (2 * S + t); };         // tile written
-    auto tfree_bar = [&](int t) { return bar + 8u * (2 * S + T + t); };   // tile consumed
-    const uint32_t tfull_bar0 = bar + 8u * (2 * S + 2 * T);              // + 8*acc
-    const uint32_t tempty_bar0 = tfull_bar0 + 8u * 8;
-    const uint32_t qfull_bar0 = tempty_bar0 + 8u * 8;                    // + 8*(2*side+slot)
-    const uint32_t qempty_bar0 = qfull_bar0 + 8u * 4;
-    const int S2 = S / 2, T2 = T / 2;   // per side
+    auto full_bar = [&](int s) { return bar + 8u * s; };                // codes and scales landed
+    auto sfa_bar = [&](int s) { return bar + 8u * (S + s); };           // key scales written
+    auto sfree_bar = [&](int s) { return bar + 8u * (2 * S + s); };     // stage consumed
+    const uint32_t tfull_bar0 = bar + 8u * (3 * S);                    // + 8 * acc
+    const uint32_t tempty_bar0 = tfull_bar0 + 8u * kAcc;
+    const uint32_t qfull_bar0 = tempty_bar0 + 8u * kAcc;               // + 8 * slot
+    const uint32_t qempty_bar0 = qfull_bar0 + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
     int* sched = reinterpret_cast<int*>(smem + L.misc + 16);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int prod = warp == kProducerWarp ? 0 : warp == kProducerWarp2 ? 1 : -1;
-    const int mmaw = warp == kMmaWarp ? 0 : warp == kMmaWarp2 ? 1 : -1;
-    const int dgrp = (warp >= kFirstDeqWarp && warp < kFirstDeqWarp + 4) ? 0
-                     : (warp >= kFirstDeqWarp2 && warp < kFirstDeqWarp2 + 4) ? 1 : -1;
-    const int egrp = (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) ? 0
-                     : warp >= kFirstEpiWarp2 ? 1 : -1;
+    const int prod = warp == 0 ? 0 : (warp == 2 || warp == 3) ? warp - 1 : -1;
 
-    if (warp == kProducerWarp) {
+    if (warp == 0) {
         const long long total = warp_total_blocks(a.context_lengths, a.groups);
         const long long s0 = range_start(total, gridDim.x, blockIdx.x);
         const long long s1 = range_start(total, gridDim.x, blockIdx.x + 1);
@@ -225,23 +256,20 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
             sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
             *abort_flag = 0;
             for (int s = 0; s < S; ++s) {
-                // expect_tx arrive (+ each lane's cp.async of scales, unless fused)
-                mbar_init(full_bar(s), a.fused ? 1 : 1 + 32);
-                mbar_init(sfree_bar(s), 4);
-            }
-            for (int t = 0; t < T; ++t) {
-                mbar_init(deq_bar(t), 4);
-                mbar_init(tfree_bar(t), 1);       // the MMA's commit
+                mbar_init(full_bar(s), 1 + 32);   // expect_tx arrival + each lane's cp.async
+                mbar_init(sfa_bar(s), 4);
+                mbar_init(sfree_bar(s), 1);       // the MMA's commit
             }
             for (int i = 0; i < kAcc; ++i) {
                 mbar_init(tfull_bar0 + 8u * i, 1);
                 mbar_init(tempty_bar0 + 8u * i, 4);
             }
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 mbar_init(qfull_bar0 + 8u * i, 4);
-                mbar_init(qempty_bar0 + 8u * i, 4);
+                mbar_init(qempty_bar0 + 8u * i, 1);
             }
             fence_mbar_init();
+            tma_prefetch_map(&kmap);
         }
     } else if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -255,109 +283,98 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
 
     if (prod >= 0) {
         // ------------------------------------------------------------ producers
+        // Tile i (counted over the CTA's range) belongs to producer i % kProducers
+        // and uses stage i % S; every producer walks every tile.
         const uint64_t policy = policy_evict_first();
         Walk w;
         w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, k = 0, prev_g = -1;   // it: tile; k: this side's tiles so far
-        RingPos sp;                        // this side's staging slot
+        int it = 0, owner = 0, prev_g = -1, win_g = -1;
+        RingPos sp;
         long long bt_row = 0;
-        // block-table entries come 32 at a time, one per lane, the next 32
-        // already in flight: lane i of `cur` holds block cur_j + i
+        // block-table entries 32 at a time, one per lane, the next 32 already
+        // in flight: lane i of `cur` holds block cur_j + i, of `nxt` cur_j + 32 + i
         int nbl = 0, cur_j = 0, cur = 0, nxt = 0;
         auto fetch = [&](int j0) {
             return j0 + lane < nbl ? __ldg(a.block_table + bt_row + j0 + lane) : 0;
         };
         bool ok = true;
         while (!w.done()) {
-            const int c = w.cnt();
-            if ((it & 1) != prod) {               // the other side's tile
-                w.advance(c);
-                ++it;
-                continue;
-            }
+            const int c = tile_blocks(w);
             const bool first = w.b != prev_g;
-            if (first) {
-                int req = __ldg(a.requests + w.b);
-                if (req < 0 || req >= a.num_requests) {
-                    if (lane == 0) atomicOr(a.status, kStatusBadRequest);
-                    req = 0;
+            prev_g = w.b;
+            if (owner == prod) {
+                if (w.b != win_g) {
+                    int req = __ldg(a.requests + w.b);
+                    if (req < 0 || req >= a.num_requests) {
+                        if (lane == 0) atomicOr(a.status, kStatusBadRequest);
+                        req = 0;
+                    }
+                    bt_row = (long long)req * a.bt_stride;
+                    nbl = blocks_of(min(w.len, a.max_context));
+                    cur_j = w.j;
+                    cur = fetch(cur_j);
+                    nxt = fetch(cur_j + 32);
+                    win_g = w.b;
                 }
-                bt_row = (long long)req * a.bt_stride;
-                nbl = blocks_of(min(w.len, a.max_context));
-                cur_j = w.j;
-                cur = fetch(cur_j);
-                nxt = fetch(cur_j + 32);
-                prev_g = w.b;
-            }
-            // the entries of blocks w.j and w.j + 1: `cur` and `nxt` hold the
-            // window [cur_j, cur_j + 64), which covers both
-            while (w.j >= cur_j + 32) {
-                cur_j += 32;
-                cur = nxt;
-                nxt = fetch(cur_j + 32);
-            }
-            const int i0 = w.j - cur_j;
-            const int e0 = __shfl_sync(0xffffffffu, cur, i0);
-            const int e1c = __shfl_sync(0xffffffffu, cur, (i0 + 1) & 31);
-            const int e1n = __shfl_sync(0xffffffffu, nxt, 0);
-            // pages of the tile below max_context
-            const int nload = (long long)w.j * kBlockKeys >= a.max_context ? 0
-                              : (c > 1 && (long long)(w.j + 1) * kBlockKeys < a.max_context) ? 2
-                                                                                             : 1;
-            long long page0 = e0, page1 = i0 < 31 ? e1c : e1n;
-            if (nload >= 1 && (page0 < 0 || page0 >= a.num_pages)) {
-                if (lane == 0) atomicOr(a.status, kStatusBadBlock);
-                page0 = 0;
-            }
-            if (nload == 2 && (page1 < 0 || page1 >= a.num_pages)) {
-                if (lane == 0) atomicOr(a.status, kStatusBadBlock);
-                page1 = 0;
-            }
-            const int s = prod * S2 + sp.idx;
-            if (lane == 0) ok = mbar_wait(sfree_bar(s), sp.phase ^ 1u, abort_flag, a.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const uint32_t dst = stage_base + (uint32_t)(2 * s) * kStagePage;
-            if (lane == 0) st_shared_v2_s32(rec_base + 8u * s, w.b, first ? kRecFirst : 0);
-            if (a.fused) {
-                // a page's codes and scales are one run of 4608 bytes
+                while (w.j >= cur_j + 32) {
+                    cur_j += 32;
+                    cur = nxt;
+                    nxt = fetch(cur_j + 32);
+                }
+                // blocks w.j .. w.j + 3 lie in the window [cur_j, cur_j + 64);
+                // the pages below max_context are a prefix of the tile
+                int page[kTileBlocks];
+                int nload = 0;
+#pragma unroll
+                for (int cc = 0; cc < kTileBlocks; ++cc) {
+                    const int i = w.j - cur_j + cc;
+                    long long pg = __shfl_sync(0xffffffffu, i < 32 ? cur : nxt, i & 31);
+                    page[cc] = 0;
+                    if (cc < c && (long long)(w.j + cc) * kBlockKeys < a.max_context) {
+                        if (pg < 0 || pg >= a.num_pages) {
+                            if (lane == 0) atomicOr(a.status, kStatusBadBlock);
+                            pg = 0;
+                        }
+                        page[cc] = (int)pg;
+                        nload = cc + 1;
+                    }
+                }
+                const int s = sp.idx;
+                if (lane == 0) ok = mbar_wait(sfree_bar(s), sp.phase ^ 1u, abort_flag, a.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t dst = stage_base + (uint32_t)s * kStageBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kStagePage);
-                    if (nload >= 1)
-                        bulk_load_stream(dst, a.key_cache + page0 * a.page_stride, kStagePage,
-                                         full_bar(s), policy);
-                    if (nload == 2)
-                        bulk_load_stream(dst + kStagePage, a.key_cache + page1 * a.page_stride,
-                                         kStagePage, full_bar(s), policy);
+                    st_shared_v2_s32(rec_base + 8u * s, w.b, first ? kRecFirst : 0);
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kPageCodes);
+#pragma unroll
+                    for (int cc = 0; cc < kTileBlocks; ++cc)
+                        if (cc < nload)
+                            tma_load_3d_stream(dst + cc * kPageCodes, &kmap, full_bar(s), 0, 0,
+                                               page[cc], policy);
                 }
-            } else {
-                // codes by bulk copies; scales (pages only 8-byte aligned) by
-                // 8-byte cp.async, two per lane per page
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kPackedPage);
-                    if (nload >= 1)
-                        bulk_load_stream(dst, a.key_cache + page0 * a.page_stride, kPackedPage,
-                                         full_bar(s), policy);
-                    if (nload == 2)
-                        bulk_load_stream(dst + kStagePage, a.key_cache + page1 * a.page_stride,
-                                         kPackedPage, full_bar(s), policy);
-                }
-                for (int cc = 0; cc < nload; ++cc) {
-                    const uint8_t* src = a.key_scales + (cc ? page1 : page0) * a.scale_stride;
-                    const uint32_t sdst = dst + (uint32_t)cc * kStagePage + kPackedPage;
-                    cp_async8(sdst + lane * 8, src + lane * 8);
-                    cp_async8(sdst + (lane + 32) * 8, src + (lane + 32) * 8);
+#pragma unroll
+                for (int cc = 0; cc < kTileBlocks; ++cc) {
+                    if (cc >= nload) break;
+                    const uint8_t* src = a.key_scales + (long long)page[cc] * a.scale_stride;
+                    const uint32_t sdst = dst + kStageCodes + cc * kPageScales;
+                    if (a.scales16) {
+                        cp_async16(sdst + 16u * lane, src + 16 * lane);
+                    } else {
+                        cp_async8(sdst + 8u * lane, src + 8 * lane);
+                        cp_async8(sdst + 8u * (lane + 32), src + 8 * (lane + 32));
+                    }
                 }
                 cp_async_arrive(full_bar(s));
             }
             w.advance(c);
             ++it;
-            ++k;
-            sp.next(S2);
+            if (++owner == kProducers) owner = 0;
+            sp.next(S);
         }
-        if (ok) {
-            // the end mark, in the next slot
-            const int s = prod * S2 + sp.idx;
+        if (ok && owner == prod) {
+            // the end mark, in the stage after the last tile
+            const int s = sp.idx;
             if (lane == 0) ok = mbar_wait(sfree_bar(s), sp.phase ^ 1u, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (ok) {
@@ -365,199 +382,188 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
                     st_shared_v2_s32(rec_base + 8u * s, -1, 0);
                     mbar_arrive_expect_tx(full_bar(s), 0u);
                 }
-                if (!a.fused) cp_async_arrive(full_bar(s));
+                cp_async_arrive(full_bar(s));
+                ++it;
             }
         }
-        if (!ok && lane == 0) {
-            for (int t = (k > S2 ? k - S2 : 0); t < k; ++t)
-                mbar_wait_drain(full_bar(prod * S2 + t % S2), (t / S2) & 1);
-        }
+        // every copy this warp issued lands before the CTA may exit, whatever
+        // the other roles did: of its stages only the last S tiles' can be in
+        // flight
         cp_async_wait_all();
-    } else if (mmaw >= 0) {
+        if (lane == 0) {
+            for (int t = (it > S ? it - S : 0); t < it; ++t)
+                if (t % kProducers == prod)
+                    mbar_wait_drain(full_bar(t % S), (uint32_t)(t / S) & 1u);
+        }
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
-        const uint32_t idesc = make_idesc(0, 0, kTileKeys, kN);   // f16 x f16 -> f32
-        Walk w;
-        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        // kg: tile within the request; qk: requests this side has tiles of
-        int it = 0, kg = 0, prev_g = -1, qk = 0, slot = 0, last = -1;
-        RingPos tp;                        // this side's f16 tile
-        bool ok = true;
-        while (!w.done()) {
-            const int c = w.cnt();
-            if (w.b != prev_g) {
-                kg = 0;
-                prev_g = w.b;
-            }
-            if ((it & 1) == mmaw) {
-                if (kg < 2) {                     // this side's first tile of the request
-                    slot = 2 * mmaw + (qk & 1);
+        if (lane == 0) {
+            const uint32_t idesc = nvfp4_idesc(128, kN);
+            Walk w;
+            w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+            int prev_g = -1, qk = 0, slot = 0, last_acc = -1;
+            uint32_t last_phase = 0;
+            RingPos sp, ap;
+            bool ok = true;
+            while (!w.done()) {
+                const int c = tile_blocks(w);
+                if (w.b != prev_g) {
+                    slot = qk & 1;
                     ok = mbar_wait(qfull_bar0 + 8u * slot, (qk >> 1) & 1, abort_flag, a.status);
                     if (!ok) break;
                     ++qk;
+                    prev_g = w.b;
                 }
-                const int tt = mmaw * T2 + tp.idx;
-                ok = mbar_wait(deq_bar(tt), tp.phase, abort_flag, a.status);
-                if (!ok) break;
-                const int acc = it % kAcc;        // this side's accumulators: it's parity
-                ok = mbar_wait(tempty_bar0 + 8u * acc, ((it / kAcc) & 1) ^ 1, abort_flag, a.status);
-                if (!ok) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t d = tmem_base + (uint32_t)(acc * kN);
-                    const uint32_t at = tmem_base + kAccCols + (uint32_t)tt * kTileCols;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t bd =
-                            smem_desc_sw128(q_base + slot * kQSlotBytes + h * kQHalfBytes);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)   // K = 16: 8 columns of A
-                            mma_f16_tmem_a(d, at + 8u * (4 * h + kk), bd + 2u * kk, idesc,
-                                           (h | kk) ? 1u : 0u);
-                    }
-                    mma_commit(tfull_bar0 + 8u * acc);
-                    mma_commit(tfree_bar(tt));    // the tile may be rewritten once these complete
-                }
-                __syncwarp();
-                last = it;
-                tp.next(T2);
-            }
-            w.advance(c);
-            ++it;
-            ++kg;
-        }
-        if (!ok && last >= 0) mbar_wait_drain(tfull_bar0 + 8u * (last % kAcc), (last / kAcc) & 1);
-    } else if (egrp >= 0) {
-        // ------------------------------------------------------------ epilogues
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const int pg = row >> 6;
-        const int key = row & 63;
-        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
-        Walk w;
-        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
-        int it = 0, prev_g = -1, len = 0, qk = 0;
-        bool ok = true;
-        while (!w.done()) {
-            const int c = w.cnt();
-            if ((it & 1) != egrp) {               // the other side's tile
-                w.advance(c);
-                ++it;
-                continue;
-            }
-            if (w.b != prev_g) {
-                prev_g = w.b;
-                len = min(__ldg(a.context_lengths + w.b), a.max_context);
-            }
-            // the request's last two tiles are the last of each side: each
-            // frees its side's q slot
-            const bool last_of_side = w.blocks_after(c) <= 2;
-            const int acc = it % kAcc;
-            ok = mbar_wait(tfull_bar0 + 8u * acc, (it / kAcc) & 1, abort_flag, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            float v[8];
-            tmem_ld8(lane_addr + (uint32_t)(acc * kN), v);
-            const int pos = (w.j + pg) * kBlockKeys + key;
-            if (pg < c && pos < len) {
-                float* dst = a.scores + (long long)w.b * G * a.scores_stride + pos;
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r < G) dst[(long long)r * a.scores_stride] = v[r];
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(tempty_bar0 + 8u * acc);
-                if (last_of_side) mbar_arrive(qempty_bar0 + 8u * (2 * egrp + (qk & 1)));
-            }
-            if (last_of_side) ++qk;
-            w.advance(c);
-            ++it;
-        }
-    } else if (dgrp >= 0) {
-        // ------------------------------------------------------------ dequantisation
-        const int t = threadIdx.x - 32 * (dgrp == 0 ? kFirstDeqWarp : kFirstDeqWarp2);
-        // key tiles: a warp may reach only its own quarter of the TMEM lanes,
-        // so the thread expands tile row (key) 32 * (warp % 4) + lane into that
-        // lane: page row / 64, row row % 64 of it
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const uint32_t row_off = (uint32_t)((row >> 6) * kStagePage + (row & 63) * kPackedRow);
-        const uint32_t sc_row_off =
-            (uint32_t)((row >> 6) * kStagePage + kPackedPage + (row & 63) * kScalesPerRow);
-        const uint32_t lane_tmem = tmem_base + ((uint32_t)(quad * 32) << 16) + kAccCols;
-        int qk = 0;
-        RingPos sp, tp;                    // this side's staging slot and f16 tile
-        bool ok = true;
-        while (true) {
-            const int s = dgrp * S2 + sp.idx, tt = dgrp * T2 + tp.idx;
-            // both waits issued before either result is needed
-            const bool got_full = mbar_try_wait(full_bar(s), sp.phase);
-            const bool got_tile = mbar_try_wait(tfree_bar(tt), tp.phase ^ 1u);
-            if (!got_full) {
+                const int s = sp.idx;
                 ok = mbar_wait(full_bar(s), sp.phase, abort_flag, a.status);
                 if (!ok) break;
+                ok = mbar_wait(sfa_bar(s), sp.phase, abort_flag, a.status);
+                if (!ok) break;
+                ok = mbar_wait(tempty_bar0 + 8u * ap.idx, ap.phase ^ 1u, abort_flag, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)ap.idx * kAccCols;
+                const uint32_t codes = stage_base + (uint32_t)s * kStageBytes;
+                const uint32_t qb = q_base + (uint32_t)slot * kQSlotBytes;
+                const uint32_t sfa = tmem_base + kSfaCol0 + 16u * s;
+                const uint32_t sfb = tmem_base + kSfbCol0 + 8u * slot;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && c <= 2) break;       // the second half holds no page
+#pragma unroll
+                    for (int kc = 0; kc < 2; ++kc)
+                        mma_nvfp4(d + kN * h, smem_desc_sw64(codes + h * kHalfCodes + 32 * kc),
+                                  smem_desc_sw64(qb + 32 * kc), idesc, sfa + 8 * h + 4 * kc,
+                                  sfb + 4 * kc, kc);
+                }
+                mma_commit(tfull_bar0 + 8u * ap.idx);
+                mma_commit(sfree_bar(s));
+                if (w.last_of_request(c)) mma_commit(qempty_bar0 + 8u * slot);
+                last_acc = ap.idx;
+                last_phase = ap.phase;
+                w.advance(c);
+                sp.next(S);
+                ap.next(kAcc);
             }
+            // the MMAs complete in order: the last commit covers them all
+            if (!ok && last_acc >= 0) mbar_wait_drain(tfull_bar0 + 8u * last_acc, last_phase);
+        }
+    } else if (warp >= kScaleWarp0 && warp < kScaleWarp0 + 4) {
+        // ------------------------------------------------------------ scales
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int t = threadIdx.x - 32 * kScaleWarp0;
+        const uint32_t lane_tmem = tmem_base + ((uint32_t)(quad * 32) << 16);
+        int qk = 0;
+        RingPos sp;
+        while (true) {
+            const int s = sp.idx;
+            if (!mbar_wait(full_bar(s), sp.phase, abort_flag, a.status)) break;
             const int2 rec = ld_shared_v2_s32(rec_base + 8u * s);
             if (rec.x < 0) break;                 // the producer's end mark
             if (rec.y & kRecFirst) {
-                // this side's first tile of group rec.x: its query rows into
-                // this side's next Q slot (rows G..15 zero)
-                const int slot = 2 * dgrp + (qk & 1);
-                ok = mbar_wait(qempty_bar0 + 8u * slot, ((qk >> 1) & 1) ^ 1, abort_flag, a.status);
-                if (!ok) break;
-                const uint32_t qh0 = q_base + slot * kQSlotBytes;
-                if (t < G) {
-                    const long long qrow = (long long)rec.x * G + t;
-                    const uint4* src = reinterpret_cast<const uint4*>(a.query + qrow * kPackedRow);
-                    const uint4 pk[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2),
-                                         __ldg(src + 3)};
-                    const uint2 sc = __ldg(
-                        reinterpret_cast<const uint2*>(a.query_scales + qrow * kScalesPerRow));
-                    dequant_row(pk, sc, qh0, qh0 + kQHalfBytes, t, 0);
-                } else if (t < kN) {
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        st_shared_v4(qh0 + sw128(t, c8), 0u, 0u, 0u, 0u);
-                        st_shared_v4(qh0 + kQHalfBytes + sw128(t, c8), 0u, 0u, 0u, 0u);
+                // the group's rows (zero beyond G) into the next Q slot: codes
+                // sign-fixed and swizzled in shared memory, scale words in
+                // every quadrant's lanes 0..15 of the slot's columns
+                const int slot = qk & 1;
+                if (!mbar_wait(qempty_bar0 + 8u * slot, ((qk >> 1) & 1) ^ 1, abort_flag, a.status))
+                    break;
+                if (t < kN * 4) {
+                    const int r = t >> 2, c = t & 3;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < G) {
+                        const long long qrow = (long long)rec.x * G + r;
+                        v = __ldg(reinterpret_cast<const uint4*>(a.query + qrow * kRowBytes) + c);
+                        const uint2 sc = __ldg(
+                            reinterpret_cast<const uint2*>(a.query_scales + qrow * kRowScales));
+                        const uint32_t m0 = scale_negative(sc, 2 * c) ? kCodeSigns : 0u;
+                        const uint32_t m1 = scale_negative(sc, 2 * c + 1) ? kCodeSigns : 0u;
+                        v.x ^= m0;
+                        v.y ^= m0;
+                        v.z ^= m1;
+                        v.w ^= m1;
                     }
+                    st_shared_v4(q_base + slot * kQSlotBytes + sw64(r, c), v);
                 }
                 fence_proxy_async_smem();
+                uint2 qs = make_uint2(0u, 0u);
+                if (lane < G)
+                    qs = __ldg(reinterpret_cast<const uint2*>(
+                        a.query_scales + ((long long)rec.x * G + lane) * kRowScales));
+                tmem_st_scales(lane_tmem + kSfbCol0 + 8u * slot, qs.x, qs.y);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qfull_bar0 + 8u * slot);
                 ++qk;
             }
-            if (!got_tile) {
-                ok = mbar_wait(tfree_bar(tt), tp.phase ^ 1u, abort_flag, a.status);
-                if (!ok) break;
-            }
-            tc_fence_after();                     // the tile's last MMA read before our stores
-            // every row: a page past the request's end or max_context holds
-            // stale bytes, which only reach accumulator rows the epilogue does
-            // not store
-            const uint32_t slot = stage_base + (uint32_t)(2 * s) * kStagePage;
-            uint4 v[4];
+            // keys row and 128 + row of the tile: page p, row kk of it.  A page
+            // that was not loaded holds stale bytes, which only reach scores
+            // the epilogue does not store.
+            const uint32_t stage = stage_base + (uint32_t)s * kStageBytes;
+            bool fixed = false;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = ld_shared_v4(slot + row_off + 16u * c);
-            const uint2 sc = ld_shared_v2_u32(slot + sc_row_off);
-            const uint32_t ta = lane_tmem + (uint32_t)tt * kTileCols;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {         // 16-byte chunk c: columns 16c..16c+15
-                const uint32_t sw = c < 2 ? sc.x : sc.y;
-                uint32_t w16[16];
-                dequant_chunk(v[c], (sw >> (16 * (c & 1))) & 0xFF, (sw >> (16 * (c & 1) + 8)) & 0xFF,
-                              w16);
-                tmem_st16(ta + 16u * c, w16);
+            for (int h = 0; h < 2; ++h) {
+                const int k = 128 * h + row, p = k >> 6, kk = k & 63;
+                const uint2 sc =
+                    ld_shared_v2_u32(stage + kStageCodes + p * kPageScales + kk * kRowScales);
+                if ((sc.x | sc.y) & kSignBits) {
+                    fix_key_signs(stage + p * kPageCodes, kk, sc);
+                    fixed = true;
+                }
+                tmem_st_scales(lane_tmem + kSfaCol0 + 16u * s + 8u * h, sc.x, sc.y);
             }
+            if (fixed) fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sfree_bar(s));        // staging slot read: refill it
-                mbar_arrive(deq_bar(tt));
+            if (lane == 0) mbar_arrive(sfa_bar(s));
+            sp.next(S);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------------------ epilogues
+        const int side = (warp - kEpiWarp0) >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+        Walk w;
+        w.init(a.context_lengths, a.groups, sb, sj, eb, ej);
+        int it = 0, prev_g = -1, len = 0;
+        while (!w.done()) {
+            const int c = tile_blocks(w);
+            if ((it & 1) == side) {
+                if (w.b != prev_g) {
+                    prev_g = w.b;
+                    len = min(__ldg(a.context_lengths + w.b), a.max_context);
+                }
+                const int acc = it % kAcc;
+                if (!mbar_wait(tfull_bar0 + 8u * acc, (uint32_t)(it / kAcc) & 1u, abort_flag,
+                               a.status))
+                    break;
+                tc_fence_after();
+                uint32_t v[2][8];
+                tmem_ld8_async(lane_addr + (uint32_t)acc * kAccCols, v[0]);
+                tmem_ld8_async(lane_addr + (uint32_t)acc * kAccCols + kN, v[1]);
+                tmem_wait_bind8(v[0]);
+                tmem_wait_bind8(v[1]);
+                float* dst = a.scores + (long long)w.b * G * a.scores_stride;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int pg = 2 * h + (row >> 6);
+                    const int pos = (w.j + pg) * kBlockKeys + (row & 63);
+                    if (pg < c && pos < len) {
+#pragma unroll
+                        for (int r = 0; r < 8; ++r)
+                            if (r < G)
+                                dst[(long long)r * a.scores_stride + pos] = __uint_as_float(v[h][r]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar0 + 8u * acc);
             }
-            sp.next(S2);
-            tp.next(T2);
+            w.advance(c);
+            ++it;
         }
     }
 
@@ -571,18 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_scores_kernel(const Nvfp4Ar
 
 }  // namespace
 
-size_t nvfp4_smem_bytes(int stages, int tiles)
-{
-    return (size_t)nvfp4_layout(stages, tiles).total + 1024;
-}
+size_t nvfp4_smem_bytes(int stages) { return (size_t)nvfp4_layout(stages).total + 1024; }
 
-cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t stream)
+cudaError_t launch_nvfp4_scores(const CUtensorMap& kmap, const Nvfp4Args& a, int num_ctas,
+                                cudaStream_t stream)
 {
-    // both rings split between the two sides; the key tiles must fit the
-    // tensor memory the kernel allocates
-    if (a.stages < 2 || (a.stages & 1) || a.tiles < 2 || (a.tiles & 1) || a.tiles > kMaxTiles)
-        return cudaErrorInvalidValue;
-    const size_t smem = nvfp4_smem_bytes(a.stages, a.tiles);
+    // each stage's scale columns must fit the tensor memory the kernel allocates
+    if (a.stages < 2 || a.stages > kMaxNvfp4Stages) return cudaErrorInvalidValue;
+    const size_t smem = nvfp4_smem_bytes(a.stages);
     static int configured_device = -1;
     static size_t configured_smem = 0;
     int dev = 0;
@@ -595,7 +597,7 @@ cudaError_t launch_nvfp4_scores(const Nvfp4Args& a, int num_ctas, cudaStream_t s
         configured_device = dev;
         configured_smem = smem;
     }
-    nvfp4_scores_kernel<<<num_ctas, kThreads, smem, stream>>>(a);
+    nvfp4_scores_kernel<<<num_ctas, kThreads, smem, stream>>>(kmap, a);
     return cudaGetLastError();
 }
 

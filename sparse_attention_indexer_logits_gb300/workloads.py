@@ -393,11 +393,14 @@ def random_e4m3_scales(g: np.random.Generator, shape, lo_exp: int = -3, hi_exp: 
 def indexer_nvfp4(group_size: int, seed: int = 6, groups: int = 256, max_context: int = 65536,
                   min_zero: int = 8, lo: int = 0, hi: int | None = None, fused: bool = True,
                   page_pad_bytes: int = 0, scale_pad_bytes: int = 0,
-                  poison: bool = True) -> Nvfp4Problem:
+                  poison: bool = True, scales: str = "positive") -> Nvfp4Problem:
     """NVFP4 single-head problem: ``groups`` groups of ``group_size`` query rows,
     one request each, lengths uniform on [lo, hi] with at least ``min_zero``
     forced zeros.  E2M1 codes are uniform over all 16 values (bytes uniform on
-    0..255) and scales are random positive E4M3 codes between 2^-3 and 2^3.
+    0..255).  ``scales``: "positive" -- random positive E4M3 codes between
+    2^-3 and 2^3; "negative" -- the same codes with the sign bit set; "all" --
+    bytes uniform on 0..255 (every E4M3 code: zeros, subnormals, negatives and
+    the two NaNs), for queries and keys alike.
     ``fused``: one buffer of pages of [4096 key bytes][512 scale bytes]
     (+ ``page_pad_bytes``); otherwise separate key and scale buffers, pages
     4096 + ``page_pad_bytes`` and 512 + ``scale_pad_bytes`` bytes apart.  With
@@ -419,10 +422,17 @@ def indexer_nvfp4(group_size: int, seed: int = 6, groups: int = 256, max_context
     for r in range(groups):
         bt[r, :need[r]] = perm[off:off + need[r]]
         off += int(need[r])
+    def draw_scales(shape):
+        if scales == "all":
+            return g.integers(0, 255, size=shape, endpoint=True).astype(np.uint8)
+        sc = random_e4m3_scales(g, shape)
+        return sc | np.uint8(0x80) if scales == "negative" else sc
+
+    assert scales in ("positive", "negative", "all")
     query = g.integers(0, 255, size=(rows, NVFP4_ROW_BYTES), endpoint=True).astype(np.uint8)
-    qscales = random_e4m3_scales(g, (rows, NVFP4_SCALES))
+    qscales = draw_scales((rows, NVFP4_SCALES))
     keys = g.integers(0, 255, size=(num_pages, NVFP4_PAGE_KEY_BYTES), endpoint=True).astype(np.uint8)
-    kscales = random_e4m3_scales(g, (num_pages, NVFP4_PAGE_SCALE_BYTES))
+    kscales = draw_scales((num_pages, NVFP4_PAGE_SCALE_BYTES))
     if poison:
         kscales[pool:] = E4M3_NAN
     fill = E4M3_NAN if poison else 0

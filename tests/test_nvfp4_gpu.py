@@ -2,12 +2,14 @@
 C ABI ("flashinfer.sdsa.indexer_scores", NVFP4 forms): group sizes 1..8,
 fused (keys then scales in one page) and separate caches, scale pages only
 8-byte aligned, padded key pages, garbage request entries for empty groups,
-max_context clipping, an out-of-range page, and the full-size workload (256
-groups, lengths U[0, 65536]) on sampled groups.
+max_context clipping, an out-of-range page, every E4M3 scale code (zeros,
+subnormals, negatives, NaN) on either operand, and the full-size workload
+(256 groups, lengths U[0, 65536]) on sampled groups.
 
 Tolerance: |gpu - oracle| <= 1e-3 * sum_d |q_d k_d| + 1e-6, the bf16 path's
-bound.  (Every dequantised value is exact in f16 and every product exact in
-fp32; only the fp32 accumulation rounds.)"""
+bound.  (Every product of two dequantised values is exact in fp32; only the
+fp32 accumulation rounds.)  A score the oracle finds NaN -- a NaN scale on
+either side reaches every score of its row or key -- must be NaN."""
 import numpy as np
 import pytest
 import torch
@@ -62,12 +64,18 @@ def check(p: W.Nvfp4Problem, got: np.ndarray, max_context=None, groups=None):
                                            p.scale_page_stride_bytes, p.block_table,
                                            p.context_lengths[gsel], p.requests[gsel], mc)
     g = got[rows]
-    written = ~np.isnan(ref)
-    err = np.abs(g.astype(np.float64) - np.where(written, ref, 0.0))
-    bound = BF16_REL * np.nan_to_num(mag) + ABS
-    bad = written & ~(err <= bound)
-    assert not bad.any(), f"{int(bad.sum())} of {int(written.sum())} scores outside tolerance"
+    lens = np.minimum(np.repeat(p.context_lengths[gsel], G), mc)
+    written = np.arange(mc)[None, :] < lens[:, None]
+    nan = written & np.isnan(ref)
+    fin = written & ~nan
+    err = np.abs(g.astype(np.float64) - np.where(fin, ref, 0.0))
+    bound = BF16_REL * np.where(fin, mag, 0.0) + ABS
+    bad = fin & ~(err <= bound)
+    assert not bad.any(), (f"{int(bad.sum())} of {int(fin.sum())} scores outside tolerance; first "
+                           f"{np.argwhere(bad)[0]}: gpu {g[bad][0]!r} oracle {ref[bad][0]!r}")
+    assert np.isnan(g[nan]).all(), f"{int((~np.isnan(g[nan])).sum())} scores should be NaN"
     assert (g[~written].view(np.uint32) == W.SENTINEL_BITS).all(), "unwritten entry modified"
+    return int(nan.sum()), int(fin.sum())
 
 
 @pytest.mark.parametrize("G", [1, 2, 3, 5, 8])
@@ -109,6 +117,39 @@ def test_out_of_range_page_is_flagged():
     pml.pml_device_status(clear=True)
     d.run(block_table=dev_tensor(bt))
     assert pml.pml_device_status(clear=True) & pml.STATUS_BAD_BLOCK
+
+
+@pytest.mark.parametrize("G,fused", [(8, True), (3, False)])
+def test_every_scale_code(G, fused):
+    """Scale bytes uniform over all 256 E4M3 codes for queries and keys: the
+    MMA reads scales without their sign, so negative ones are applied to the
+    codes; NaN scales make their rows' or keys' scores NaN."""
+    p = W.indexer_nvfp4(G, seed=430 + G, groups=10, max_context=1500, min_zero=1, lo=200,
+                        fused=fused, scales="all")
+    nans, finite = check(p, Nvfp4Device(p).run())
+    assert nans > 0 and finite > 0
+    assert pml.pml_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("G", [2, 8])
+def test_negative_scales(G):
+    """Every scale of both operands negative (the sign bits flip the codes of
+    their blocks on the way to the tensor cores)."""
+    p = W.indexer_nvfp4(G, seed=440 + G, groups=8, max_context=1300, min_zero=1,
+                        scales="negative")
+    check(p, Nvfp4Device(p).run())
+    assert pml.pml_device_status(clear=True) == 0
+
+
+def test_one_negative_key_block():
+    """A single negative scale block in one key among positive ones."""
+    p = W.indexer_nvfp4(4, seed=450, groups=3, max_context=400, min_zero=0, lo=300,
+                        poison=False)
+    page = int(p.block_table[1, 2])
+    at = p.scale_off + page * p.scale_page_stride_bytes + 37 * 8 + 5   # key 37, block 5
+    p.scale_buf[at] |= 0x80
+    got = Nvfp4Device(p).run()
+    check(p, got)
 
 
 @pytest.mark.parametrize("G", [1, 8])
