@@ -599,7 +599,7 @@ def main():
             "dtype": (("e4m3 x e4m3 -> f32" + (" -> bf16 out" if out_dtype == torch.bfloat16 else ""))
                       if is_fp8 else
                       ("mxfp4 (e2m1 x e8m0/32) -> f16 or bf16 x same -> f32 -> bf16 out" if is_mx else
-                       "nvfp4 (e2m1 x e4m3/16) -> f16 x f16 -> f32" if is_nvfp4
+                       "nvfp4 (e2m1 x e2m1, e4m3 scale per 16, block-scaled MMA) -> f32" if is_nvfp4
                                       else ("f32 logits -> int32 indices" if is_topk
                                             else "bf16 x bf16 -> f32"))),
             "data": "synthetic (seeded generators; no public dataset on the pages)",
