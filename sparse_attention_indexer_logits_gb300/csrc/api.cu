@@ -340,7 +340,27 @@ int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_
         if (stages > kMaxMxfp4Stages) stages = kMaxMxfp4Stages;
         (nn == 1 ? a.stages : a.stages2) = stages;
     }
-    e = launch_mxfp4_logits(a, num_ctas, static_cast<cudaStream_t>(stream));
+    // the codes of block P: 64 rows of 64 bytes at P * 4352; the query rows:
+    // 64 bytes each, 64 (one slot's heads) per copy; both land with the
+    // 64-byte swizzle the MMA reads
+    CUtensorMap kmap, qmap;
+    {
+        const uint64_t dims[3] = {(uint64_t)kHeadDim / 2, (uint64_t)kBlockKeys, (uint64_t)num_blocks};
+        const uint64_t strides[2] = {(uint64_t)kHeadDim / 2, (uint64_t)kMxfp4BlockBytes};
+        const uint32_t box[3] = {(uint32_t)kHeadDim / 2, (uint32_t)kBlockKeys, 1};
+        e = encode_tiled(kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_cache, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_64B);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)kHeadDim / 2, (uint64_t)batch * next_n * kMxfp4Heads};
+        const uint64_t strides[1] = {(uint64_t)kHeadDim / 2};
+        const uint32_t box[2] = {(uint32_t)kHeadDim / 2, (uint32_t)kMxfp4Heads};
+        e = encode_tiled(qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_64B);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_mxfp4_logits(kmap, qmap, a, num_ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PML_OK : cuda_fail(e);
 }
 

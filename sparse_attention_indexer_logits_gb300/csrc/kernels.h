@@ -124,7 +124,8 @@ cudaError_t launch_bf16_scores(const CUtensorMap& kmap, const CUtensorMap& qmap,
 cudaError_t launch_nvfp4_scores(const CUtensorMap& kmap, const Nvfp4Args& a, int num_ctas,
                                 cudaStream_t stream);
 // The MXFP4 logits: one launch per pass of at most two query slots.
-cudaError_t launch_mxfp4_logits(const Mxfp4Args& a, int num_ctas, cudaStream_t stream);
+cudaError_t launch_mxfp4_logits(const CUtensorMap& kmap, const CUtensorMap& qmap,
+                                const Mxfp4Args& a, int num_ctas, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int batch, int num_ctas, int32_t* meta,
                             cudaStream_t stream);
