@@ -232,6 +232,8 @@ int fp8_logits_call(const uint8_t* q, const uint8_t* kv_fused, int64_t num_block
     const size_t per_stage = fp8_smem_bytes(next_n, num_heads, 1) - fixed;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
     if (stages > kMaxFp8Stages) stages = kMaxFp8Stages;
+    // an even count: the kernel's two producers take the stages in turn
+    stages &= ~1;
     if (stages < 2) return PML_ERR_UNSUPPORTED;
     a.stages = stages;
 

@@ -18,16 +18,18 @@
 //             m of every stage; four tcgen05.mma kind::f8f6f4 (K = 32 each)
 //             compute S = K (128 x 128) * Q^T into the stage's accumulator
 //             (TMEM lanes = keys, columns = next_n*H), then tcgen05.commit.
-//   warps 1-2 producers (whole warps, stages alternate between them).
-//             Block-table entries come 32 at a time in one coalesced load,
-//             double-buffered in registers and handed out by shuffles.  Per
-//             stage the owner waits for the slot, publishes a stage
+//   warps 1-2 producers, stage i to warp 1 + i % 2: both walk the CTA's
+//             range in windows of up to 32 sub-tiles, one per lane (request,
+//             blocks and block-table entries read by the lanes in parallel);
+//             per own stage the warp waits for the slot, publishes a stage
 //             descriptor (per sub-tile: request, block, count, length,
-//             flags) in shared memory, and lanes 0..3 issue in parallel the
-//             TMA copy of each block's keys (8 KB, 3-D tensor map, 128-byte
+//             flags) in shared memory, and the owning lanes issue the TMA
+//             copy of each block's keys (8 KB, 3-D tensor map, 128-byte
 //             swizzle) and the bulk copy of its 64 scales (256 B).  Per
-//             request, the q rows (next_n*H x 128 e4m3) and weights.  After
-//             the last stage an end marker.
+//             request starting in an own stage, the q rows (next_n*H x 128
+//             e4m3) and weights.  After the last stage an end marker.  One
+//             warp issuing every copy (eight per 256 keys) is slower than the
+//             stage's share of HBM time, hence two.
 //   warps 4-11 epilogue, two warpgroups: with KT = 2 group g takes sub-tile g
 //             of every stage (all slots), with KT = 1 both take the one
 //             sub-tile and split the slots (t = g, g+2).  Each thread owns one
@@ -57,7 +59,7 @@ namespace fp8 {
 constexpr int kSubKeyBytes = kTileKeys * kHeadDim;     // 16 KB: one sub-tile of keys
 constexpr int kSubScaleBytes = kTileKeys * 4;          // 512 B
 constexpr int kMmaWarp = 0;                            // also allocates TMEM
-constexpr int kProducerWarp = 1;                       // warp 2 has no role
+constexpr int kProducers = 2;                          // warps 1, 2: stage i is warp 1 + i % 2's
 constexpr int kMmaWarp2 = 3;                           // issues sub-tile 1 of each stage
 constexpr int kFirstEpiWarp = 4;
 // Two epilogue warpgroups: one per sub-tile when a stage holds two, else
@@ -298,10 +300,11 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
     // The next call may be placed on SMs as this grid leaves them; nothing
     // here touches global memory before grid_dependency_wait.
     allow_dependent_launch();
-    const bool producer = warp == kProducerWarp;
-    // The producer computes its range and its first window (block-table
-    // reads included) before the CTA-wide barrier, so that these global round
-    // trips overlap the TMEM allocation and the barrier set-up.
+    const int prod = (warp == 1 || warp == 2) ? warp - 1 : -1;
+    const bool producer = prod >= 0;
+    // The producers compute their range and first window (block-table reads
+    // included) before the CTA-wide barrier, so that these global round trips
+    // overlap the TMEM allocation and the barrier set-up.
     int sb = 0, sj = 0, eb = 0, ej = 0;
     Window win;
     if (producer) {
@@ -351,9 +354,15 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
         if (producer) {
             // ------------------------------------------------------------ producer
             const uint64_t policy = policy_evict_first();
+            // Both producers walk every stage of the CTA's range (windows
+            // included); producer p publishes stage i (counted from 0) when
+            // i % 2 == p, with the q tiles of the requests starting in it.
+            // One warp issuing every copy of a stage (eight per 256 keys)
+            // takes longer than the stage's share of HBM time.
             uint32_t s = 0, ph = 0;
             int qbase = 0;                  // requests started in earlier windows
-            int issued = 0, q_issued = 0;   // stages published, q tiles requested
+            int issued = 0, q_issued = 0;   // stages walked, q tiles of the range
+            int own_q0 = -1, own_q1 = -1;   // this warp's latest q tile per slot
             bool ok = true;
             // TMA of one block's keys (8 KB, 128-byte swizzle) and bulk copy of
             // its 64 scales into stage s
@@ -375,13 +384,14 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 for (int st = 0; st < stages_here; ++st) {
                     const int o0 = st * KT;
                     const int i = lane - o0;                 // sub-tile slot this lane fills
-                    const bool own = i >= 0 && i < KT && lane < win.n;
+                    const bool mine = issued % kProducers == prod;
+                    const bool own = mine && i >= 0 && i < KT && lane < win.n;
                     // q / weights of each request starting in this stage, in order
 #pragma unroll
                     for (int k = 0; k < KT; ++k) {
                         const int ol = o0 + k;
                         if (ol < win.n && ((win.first_mask >> ol) & 1u)) {
-                            if (lane == ol) {
+                            if (mine && lane == ol) {
                                 const int slot = qidx & 1;
                                 ok = mbar_wait<kCallWait>(qempty_bar0 + 8u * slot,
                                                           ((qidx >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_limit_ns);
@@ -396,17 +406,21 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                             }
                             ok = __shfl_sync(0xffffffffu, ok, ol);
                             if (!ok) break;
+                            if (mine) {
+                                if (q_issued & 1) own_q1 = q_issued;
+                                else own_q0 = q_issued;
+                            }
                             ++q_issued;
                         }
                     }
                     if (!ok) break;
-                    if (lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status, a.wait_limit_ns);
+                    if (mine && lane == 0) ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status, a.wait_limit_ns);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     // publish the stage: each owner lane its sub-tile, lane 0 the rest
                     // (not at all for the stage a test asks to leave out: the roles
                     // waiting on it then run out of time and the CTA aborts)
-                    const bool publish = issued != a.drop_stage;
+                    const bool publish = mine && issued != a.drop_stage;
                     StageDesc& sd = descs[s];
                     if (own && publish) {
                         const int meta = win.cnt | (win.first ? kMetaFirst : 0) |
@@ -444,8 +458,9 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 win = nxt;
             }
             bool end_written = false;
-            if (ok && lane == 0) {
-                // end marker for the MMA and epilogue warps, in the stage after the last one
+            if (ok && lane == 0 && issued % kProducers == prod) {
+                // end marker for the MMA and epilogue warps, in the stage after the
+                // last one, from the producer whose turn it is
                 ok = mbar_wait<kCallWait>(empty_bar0 + 8u * s, ph ^ 1, abort_flag, a.status, a.wait_limit_ns);
                 if (ok) {
                     *reinterpret_cast<int4*>(&descs[s].sub[0]) = make_int4(0, 0, 0, kStageEnd);
@@ -459,16 +474,19 @@ __global__ void __launch_bounds__(threads_of(NN), 1)
                 // phases have completed already).  The end marker's stage is left
                 // out: its barrier has moved on, and the copies of its earlier use
                 // were consumed before the marker could take the stage.
+                // With S even, stage T - S (T = stages walked), whose slot the
+                // marker takes, belongs to the marker's producer, which leaves it
+                // out; the other producer owns none of the two.
                 const int depth = end_written ? S - 1 : S;
-                uint32_t ds = s, dph = ph;
-                for (int t = 0; t < issued && t < depth; ++t) {
-                    if (ds == 0) { ds = S; dph ^= 1; }
-                    --ds;
-                    if (issued - 1 - t != a.drop_stage)   // that one holds no copies
-                        mbar_wait_drain<kCallWait>(full_bar0 + 8u * ds, dph, a.wait_limit_ns);
-                }
-                for (int qc = (q_issued > 2 ? q_issued - 2 : 0); qc < q_issued; ++qc)
-                    mbar_wait_drain<kCallWait>(qfull_bar0 + 8u * (qc & 1), (qc >> 1) & 1, a.wait_limit_ns);
+                for (int t = (issued > depth ? issued - depth : 0); t < issued; ++t)
+                    if (t % kProducers == prod && t != a.drop_stage)   // that one holds no copies
+                        mbar_wait_drain<kCallWait>(full_bar0 + 8u * (uint32_t)(t % S),
+                                                   (uint32_t)(t / S) & 1u, a.wait_limit_ns);
+                // of its q tiles only those of the range's last two requests
+                if (own_q0 >= q_issued - 2 && own_q0 >= 0)
+                    mbar_wait_drain<kCallWait>(qfull_bar0, (uint32_t)(own_q0 >> 1) & 1u, a.wait_limit_ns);
+                if (own_q1 >= q_issued - 2 && own_q1 >= 0)
+                    mbar_wait_drain<kCallWait>(qfull_bar0 + 8u, (uint32_t)(own_q1 >> 1) & 1u, a.wait_limit_ns);
             }
         } else if (warp == kMmaWarp || warp == kMmaWarp2) {
             // ------------------------------------------------------------ MMA issuers
@@ -649,6 +667,9 @@ cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& qmap, const Fp8Ar
                    int num_ctas, cudaStream_t stream)
 {
     constexpr int N = n_pad_of(NN, H);
+    // the two producers take the stages in turn; the end marker's stage rule
+    // in their drain needs an even count
+    if (a.stages < 2 || (a.stages & 1)) return cudaErrorInvalidValue;
     const size_t smem = (size_t)layout(N, NN, H, a.stages).total + 1024;
     static int configured_device = -1;
     static size_t configured_smem = 0;
