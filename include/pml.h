@@ -194,8 +194,12 @@ int pml_indexer_scores_bf16(const uint16_t* query, int rows, const uint16_t* key
  * A row of 128 values is 64 bytes of E2M1 codes, two to a byte (element d in
  * byte d/2; the low nibble holds the even element), and 8 E4M3 scale codes,
  * scale j applying to elements 16j .. 16j+15: value = E2M1(code) * E4M3(scale).
- * Groups, lengths, requests, the written region and the status bits are
- * those of pml_indexer_scores_bf16.
+ * Every E4M3 code is accepted (negative scales negate their block; 0x7F and
+ * 0xFF are NaN and make every score of their row or key NaN).  Groups,
+ * lengths, requests, the written region and the status bits are those of
+ * pml_indexer_scores_bf16.  Every product of two values is exact in fp32
+ * (the block-scaled tensor cores take codes and scales as stored); only the
+ * sums round.
  *
  * query           uint8 [rows, 64], 16-byte aligned
  * query_scales    uint8 [rows, 8] (E4M3), 8-byte aligned
@@ -269,20 +273,21 @@ int pml_fp8_paged_mqa_logits_wait_test(const uint8_t* q, const uint8_t* kv_fused
  *            as two passes over the cache, slots 0-1 then the rest, each
  *            its own launch on `stream`)
  *
- * Method: every row (a key, or one head of one query slot) is split into a
- * power of two, 2^(E - 127) with E its largest group exponent, and its codes
- * shifted down by each group's distance to E.  The shifted codes are exact
- * 16-bit operands (f16 while a row's four scales lie within 23 binades, bf16
- * up to 132) and the tensor cores form their dot products exactly in fp32;
- * the key's and the query rows' powers of two are applied afterwards, the
- * rows' folded into the head weights relative to the slot's largest one.  So
- * each logit is its exact value up to fp32 rounding of the sums -- a logit
- * beyond the output type's range is +-inf -- except where a key's and a
- * query row's scale spreads together exceed 124 binades, when products
- * smaller than 2^-124 of the two rows' largest may be dropped, or a head's
- * largest scale lies more than 100 binades below the slot's largest: both
- * set PML_STATUS_FP4_INEXACT.  An E8M0 NaN scale (0xFF) makes its group
- * NaN, and a NaN dot product is rectified to 0.
+ * Method: every row (a key, or one head of one query slot) has a frame
+ * 2^(E - 127), E its largest group exponent.  The block-scaled tensor cores
+ * take the codes as stored and each group's scale relative to its row's
+ * frame (2^(e - E), at most 1), so every product of a key group and a query
+ * group is exact in fp32 and only the sums round; the key's and the query
+ * rows' frames are applied afterwards, the rows' folded into the head weights
+ * relative to the slot's largest one.  So each logit is its exact value up
+ * to fp32 rounding of the sums -- a logit beyond the output type's range is
+ * +-inf -- except where a key's and a query row's scale spreads together
+ * exceed 124 binades, when products smaller than 2^-124 of the two rows'
+ * frames may be rounded or dropped (a group more than 127 binades below its
+ * row's frame is dropped), or a head's largest scale lies more than 100
+ * binades below the slot's largest: both set PML_STATUS_FP4_INEXACT.  An
+ * E8M0 NaN scale (0xFF) makes its group NaN, and a NaN dot product is
+ * rectified to 0.
  */
 int pml_fp4_paged_mqa_logits(const uint8_t* q, const uint8_t* q_sf, const uint8_t* kv_cache,
                              int64_t num_blocks, const float* weights, const int32_t* seq_lens,

@@ -3,14 +3,14 @@
 folded into the dequantised operands, 64 heads of 128, bf16 output by
 default).
 
-The GPU path splits every row into a power of two (its largest group scale)
-and codes shifted by each group's distance to it -- exact f16 or bf16
-operands -- so the tensor cores form each row pair's dot product from exact
-products in fp32, and the powers of two are applied afterwards.  Its bound
-is the fp8 one: |gpu - oracle| <= 1e-3 * mag + 1e-6 (mag = sum_h |w| |q.k|),
-plus half a bf16 ulp (<= 2^-9 of the value, 2^-8 taken) for bf16 output.  A
-logit beyond the output type's range must be the infinity of its sign (either
-is accepted within 2^-7 of the largest finite value).
+The GPU path gives every row (a key, or one head of a slot) a frame, its
+largest E8M0 exponent, and hands the block-scaled tensor cores the codes as
+stored with the scales relative to the frame, so each block's terms are exact
+in fp32 and the frames are applied after the weighted sum.  Its bound is the
+fp8 one: |gpu - oracle| <= 1e-3 * mag + 1e-6 (mag = sum_h |w| |q.k|), plus
+half a bf16 ulp (<= 2^-9 of the value, 2^-8 taken) for bf16 output.  A logit
+beyond the output type's range must be the infinity of its sign (either is
+accepted within 2^-7 of the largest finite value).
 
 The scale domain is the pages' whole one: E8M0 exponents over every finite
 value (2^-127 .. 2^127), each row's four groups drawn independently.  Where
@@ -107,9 +107,9 @@ def test_decode_shape_batch8():
 
 @pytest.mark.parametrize("next_n", [1, 2, 4])
 def test_scales_over_62_binades_exact(next_n):
-    """Group scales 2^-31 .. 2^31 on both operands: rows too wide for f16,
-    every tile in bf16; the spreads add up to at most 124 binades, so the
-    status word stays clean."""
+    """Group scales 2^-31 .. 2^31 on both operands: the spreads add up to at
+    most 124 binades, so every block term is exact and the status word stays
+    clean."""
     p = W.mxfp4_problem(f"mx_w62_n{next_n}", [700, 129, 64, 1500], next_n, seed=70 + next_n,
                         lo_exp=-31, hi_exp=31)
     out, status = run(p, torch.float32)
@@ -154,9 +154,10 @@ def test_wide_keys_narrow_queries():
     check(p, out)
 
 
-def test_tiles_of_either_format():
-    """Narrow scales except for a few keys with a group 30 binades down: the
-    128-key tiles holding them run in bf16, the others in f16, in one call."""
+def test_keys_with_one_far_group():
+    """Narrow scales except for a few keys with a group 30 binades below its
+    row's frame, in one call: their relative scales reach far below the
+    others' and stay exact."""
     p = W.mxfp4_problem("mx_mixed", [1024, 700], 1, seed=84, poison=False)
     for blk, key in ((p.block_table[0, 3], 5), (p.block_table[0, 9], 63), (p.block_table[1, 2], 0)):
         p.kv[blk, W.MXFP4_BLOCK_CODE_BYTES + 4 * key + 1] = 127 - 30
