@@ -455,7 +455,8 @@ int pml_indexer_scores_nvfp4(const uint8_t* query, const uint8_t* query_scales, 
     const size_t per_stage = nvfp4_smem_bytes(1) - fixed;
     if ((size_t)dev.smem_optin < fixed + 2 * per_stage) return PML_ERR_UNSUPPORTED;
     int stages = (int)(((size_t)dev.smem_optin - fixed) / per_stage);
-    a.stages = stages > kMaxNvfp4Stages ? kMaxNvfp4Stages : stages;
+    if (stages > kMaxNvfp4Stages) stages = kMaxNvfp4Stages;
+    a.stages = stages - stages % kNvfp4Producers;   // the kernel's producers share the ring
     // the codes of page P: 64 rows of 64 bytes at P * page_stride, landing
     // with the 64-byte swizzle the MMA reads
     CUtensorMap kmap;

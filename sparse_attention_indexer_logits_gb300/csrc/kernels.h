@@ -47,8 +47,10 @@ struct Bf16Args {
     int q_box_rows;
 };
 
-// Stages of the NVFP4 kernel: each has 16 tensor-memory columns of key scales.
+// Stages of the NVFP4 kernel: each has 16 tensor-memory columns of key scales;
+// their count is a multiple of the kernel's producer warps.
 constexpr int kMaxNvfp4Stages = 20;
+constexpr int kNvfp4Producers = 3;
 
 struct Nvfp4Args {
     const uint8_t* query;          // [rows][64] packed E2M1

@@ -76,7 +76,7 @@ constexpr uint32_t kSfaCol0 = kAcc * kAccCols;             // 16 columns per sta
 constexpr uint32_t kSfbCol0 = kSfaCol0 + 16u * kMaxNvfp4Stages;   // 8 columns per Q slot
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSfbCol0 + 16 <= kTmemCols, "scale columns beyond the allocation");
-constexpr int kProducers = 3;       // warps 0, 2, 3: tile i is producer i % 3's
+constexpr int kProducers = kNvfp4Producers;   // warps 0, 2, 3: tile i is producer i % 3's
 constexpr int kMmaWarp = 1;
 constexpr int kScaleWarp0 = 4;      // a whole warpgroup: warp w writes lane quadrant w % 4
 constexpr int kEpiWarp0 = 8;        // warps 8-11 even tiles, 12-15 odd tiles
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every copy this warp issued lands before the CTA may exit, whatever
         // the other roles did: of its stages only the last S tiles' can be in
-        // flight
+        // flight (S a multiple of kProducers: see the launch)
         cp_async_wait_all();
         if (lane == 0) {
             for (int t = (it > S ? it - S : 0); t < it; ++t)
@@ -582,8 +582,12 @@ size_t nvfp4_smem_bytes(int stages) { return (size_t)nvfp4_layout(stages).total 
 cudaError_t launch_nvfp4_scores(const CUtensorMap& kmap, const Nvfp4Args& a, int num_ctas,
                                 cudaStream_t stream)
 {
-    // each stage's scale columns must fit the tensor memory the kernel allocates
-    if (a.stages < 2 || a.stages > kMaxNvfp4Stages) return cudaErrorInvalidValue;
+    // each stage's scale columns must fit the tensor memory the kernel
+    // allocates; a multiple of kProducers keeps stage T - S (T = tiles), whose
+    // slot the end mark takes, with the producer that writes the mark, which
+    // is the one that leaves it out of its drain
+    if (a.stages < kProducers || a.stages > kMaxNvfp4Stages || a.stages % kProducers != 0)
+        return cudaErrorInvalidValue;
     const size_t smem = nvfp4_smem_bytes(a.stages);
     static int configured_device = -1;
     static size_t configured_smem = 0;
