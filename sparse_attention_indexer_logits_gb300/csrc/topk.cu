@@ -11,25 +11,36 @@
 //
 // A row is one cluster of kSlices CTAs; CTA s of the cluster holds the
 // slice [s*chunk, min(lim, (s+1)*chunk)) of the row, chunk = ceil(lim /
-// kSlices), in shared memory when it fits.
-//   1. Radix select of the exact key T of the K-th largest candidate (K =
-//      min(k, lim)), 8 bits per pass: each CTA histograms its slice, and
-//      every CTA sums the kSlices histograms through distributed shared
-//      memory (two histogram buffers, alternating, so one cluster barrier
-//      per pass suffices).
-//   2. Each CTA counts its keys above T and equal to T; after an exchange of
-//      the counts it knows where its candidates go: all its keys above T,
-//      and the first ones equal to T in position order that the slices
-//      before it left over (K - #above in all).
-//   3. Each CTA sorts its candidates, (key, ~position) descending, in its own
-//      shared memory; after a cluster barrier it copies every other CTA's
-//      sorted list next to its own and places each of its candidates at its
-//      rank: its index in its own list plus, for every other list, the
-//      number of entries there that come before it (binary search).
-//      Candidates are distinct, so the ranks are a permutation of 0..K-1.
-// Every CTA of a cluster takes the same path (K is the row's), so they all
-// meet at every cluster barrier; the last one keeps each CTA's shared memory
-// alive until the others are done reading it.
+// kSlices), as order keys in shared memory when it fits.  Every exchange
+// between the CTAs is a push: a CTA stores into the others' shared memory
+// (distributed shared memory) and one cluster barrier later they read it
+// locally.
+//   1. Radix select, 8 bits per pass from the top: each CTA histograms its
+//      slice and pushes the histogram to every CTA, each CTA sums the eight
+//      and finds the bin that holds the K-th largest key (K = min(k, lim)).
+//      The passes stop as soon as the keys at or above that bin's lower
+//      edge lo number at most K + kCapExtra -- after two passes on
+//      Gaussian-like rows -- and these keys, sorted, give the answer in
+//      their first K places.  Otherwise (many keys equal to the K-th one)
+//      the four passes give it exactly, T; the keys above T are sorted
+//      and the first keys equal to T in position order fill the rest.
+//   2. The keys to sort are cut into at most 256 bins, ascending in key:
+//      each top-8-bit digit that holds some of them (counted by the first
+//      pass) gets a share of the bins in proportion to its count, bins of
+//      equal power-of-two width over its range (from lo, or the digit's
+//      start, to the digit's end or the row's largest key).  The CTAs push
+//      and sum the bins' histograms, which gives each bin's place in the
+//      output; the bins are dealt out in descending order to the CTAs in
+//      runs of about an eighth of the keys each.  Each CTA stores every one
+//      of its keys, packed with its position, into the shared memory of
+//      the bin's owner at the bin's place.
+//   3. After a last cluster barrier each CTA ranks the entries it received:
+//      an entry's place is the number of keys in higher bins plus the
+//      number of entries of its own bin that come before it (a bin holds a
+//      few dozen entries on such rows).
+// All CTAs of a cluster take the same path (their histograms are the
+// row's), so they meet at every cluster barrier; none touches another's
+// shared memory after the last, so none waits for the others to leave.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -42,6 +53,8 @@ namespace {
 constexpr int kSlices = 8;          // CTAs per row (a portable cluster size)
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 256;          // radix digits; bins of the keys to sort
+constexpr int kCapExtra = 256;      // keys past K a row may take into the sort
 
 // Keys and values stay integer bit patterns throughout: a float register can
 // be canonicalised on its way (a NaN payload or sign lost), and the order
@@ -62,6 +75,15 @@ __device__ __forceinline__ unsigned long long pack_cand(uint32_t key, int p)
     return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)p);
 }
 
+// Bin of a key to sort (key >= lo): its digit D = key >> 24 has bins from
+// first[D] = info[D] & 0xFFFF on, each 2^(info[D] >> 16) keys wide from
+// base[D].
+__device__ __forceinline__ int key_bin(uint32_t key, const uint32_t* base, const int* info)
+{
+    const int d = (int)(key >> 24), i = info[d];
+    return (i & 0xFFFF) + (int)((unsigned long long)(key - base[d]) >> (i >> 16));
+}
+
 __device__ __forceinline__ uint32_t cluster_rank()
 {
     uint32_t r;
@@ -70,58 +92,53 @@ __device__ __forceinline__ uint32_t cluster_rank()
 }
 
 // Every thread of every CTA of the cluster arrives; shared-memory writes
-// before it are visible to the cluster after it.
+// before it (local or into another CTA) are visible to the cluster after it.
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank)
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
-    uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Address of the shared-memory location `local` (a shared-window address of
+// this CTA) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t remote_addr(uint32_t local, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
     return ra;
 }
 
-// Loads from another CTA's shared memory.  They carry no memory clobber, so
-// that several can be in flight at once; being volatile they stay after the
-// cluster barrier that precedes them, and a later write of this CTA's own
-// shared memory does not alias anything they read.
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v)
 {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr)
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
 {
-    uint4 v;
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
+    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr)
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v)
 {
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr));
-    return v;
+    asm volatile("st.shared::cluster.u64 [%0], %1;" :: "r"(addr), "l"(v) : "memory");
 }
 
-// The slice's candidates: from the shared-memory copy when it fits
-// (`cached`), else from global memory.
-struct SliceSource {
+// The slice's order keys: from the shared-memory copy when it fits
+// (`cached`), else converted from global memory.
+struct SliceKeys {
     const uint32_t* gx;    // the row, position 0
-    const uint32_t* sx;    // the copy, slice position 0
+    const uint32_t* sk;    // the copy, slice position 0
     int s0;
     bool cached;
     __device__ __forceinline__ uint32_t operator()(int p) const
     {
-        return cached ? sx[p - s0] : __ldg(gx + p);
+        return cached ? sk[p - s0] : order_key(__ldg(gx + p));
     }
 };
 
@@ -150,20 +167,37 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* buf, int& total)
     return before + incl - v;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems, int sort_cap)
+// This CTA's 256-bin histogram into row `rank` of inbox `box` (a shared-window
+// address) of every CTA of the cluster: thread t stores 16 bytes into two
+// CTAs.
+__device__ __forceinline__ void push_hist(const uint32_t* hist, uint32_t box, uint32_t rank)
 {
-    __shared__ __align__(16) unsigned int hist[2][256];
-    __shared__ __align__(16) unsigned int merged[256];            // the slices' histograms summed
-    __shared__ int slice_counts[4][kSlices];                      // counts[] of every slice
-    __shared__ int counts[4];        // {above T, equal to T, list offset, list length} of this CTA
-    __shared__ int sel[2];
+    const int tid = threadIdx.x, part = tid & 63, c0 = 2 * (tid >> 6);
+    const uint4 v = reinterpret_cast<const uint4*>(hist)[part];
+    const uint32_t local = box + (rank * kBins + 4 * part) * 4;
+    st_cluster_v4(remote_addr(local, (uint32_t)c0), v);
+    st_cluster_v4(remote_addr(local, (uint32_t)c0 + 1), v);
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems, int cap)
+{
+    __shared__ __align__(16) uint32_t inbox[2][kSlices][kBins];   // the slices' histograms
+    __shared__ __align__(16) uint32_t hist[kBins];   // this CTA's histogram, then the bins' slot counters
+    __shared__ int abv[kBins];        // summed histogram (radix passes); keys in higher bins (sort)
+    __shared__ int base_me[kBins];    // where this CTA's keys of a bin go in the owner's entries
+    int* const h1 = base_me;          // before it: the row's first-pass histogram
+    __shared__ uint32_t dbase[kBins];  // per digit: lowest key of its bins
+    __shared__ int dinfo[kBins];       // per digit: first bin | bin width bits << 16
+    __shared__ uint32_t eq_in[kSlices];   // the slices' counts of keys equal to T
+    __shared__ uint32_t max_in[kSlices];  // the slices' largest keys
+    __shared__ uint32_t wmax[kWarps];
+    __shared__ int sel[3];
+    __shared__ int span[2];
     __shared__ int scan_buf[kWarps];
     extern __shared__ __align__(16) uint8_t dyn[];
-    // dynamic: the sorted list (sort_cap entries), every CTA's lists
-    // (k entries), the slice copy (cache_elems)
-    unsigned long long* own = reinterpret_cast<unsigned long long*>(dyn);
-    unsigned long long* all = own + sort_cap;
-    uint32_t* slice_copy = reinterpret_cast<uint32_t*>(all + a.k);
+    // dynamic: the received entries (cap), the slice's keys (cache_elems)
+    unsigned long long* recv = reinterpret_cast<unsigned long long*>(dyn);
+    uint32_t* sk = reinterpret_cast<uint32_t*>(recv + cap);
 
     const int row = blockIdx.x / kSlices;
     const uint32_t rank = cluster_rank();
@@ -174,60 +208,98 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
     int lim = len > 0 ? min(len - a.next_n + t + 1, a.max_context) : 0;
     if (lim < 0) lim = 0;
     const int K = min(a.k, lim);
+    int32_t* oi = a.indices + (long long)row * a.indices_stride;
+    uint32_t* ov = a.values ? reinterpret_cast<uint32_t*>(a.values) + (long long)row * a.values_stride
+                            : nullptr;
+    if (rank == 0) {
+        for (int i = K + tid; i < a.k; i += kThreads) {
+            oi[i] = -1;
+            if (ov) ov[i] = 0xFF800000u;     // -inf
+        }
+    }
+    if (K == 0) return;                      // the whole cluster: no barrier follows
+
     const int chunk = (lim + kSlices - 1) / kSlices;
     const int s0 = min(lim, (int)rank * chunk), s1 = min(lim, s0 + chunk);
     const uint32_t* gx =
         reinterpret_cast<const uint32_t*>(a.logits) + (long long)row * a.logits_stride;
     const bool cached = chunk <= cache_elems;
-    if (cached) {
-        for (int p = s0 + tid; p < s1; p += kThreads) slice_copy[p - s0] = __ldg(gx + p);
-    }
-    const SliceSource x{gx, slice_copy, s0, cached};
+    const uint32_t box0 = smem_addr(&inbox[0][0][0]);
 
-    // ---------------------------------------------------------------- 1. radix select
-    uint32_t prefix = 0, mask = 0;
-    int need = K;
-    int buf = 0;
-    for (int shift = 24; shift >= 0 && K > 0; shift -= 8, buf ^= 1) {
-        hist[buf][tid] = 0u;                       // kThreads == 256 bins
-        merged[tid] = 0u;
-        __syncthreads();
-        // four positions per thread per step, loaded before any is counted
-        for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
-            int bins[4];
+    // ------------------------------------------------ the slice's keys and the first histogram
+    hist[tid] = 0u;
+    __syncthreads();
+    uint32_t kmax = 0u;
+    for (int p0 = s0; p0 < s1; p0 += 8 * kThreads) {
+        uint32_t v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int p = p0 + u * kThreads + tid;
-                const uint32_t key = p < s1 ? order_key(x(p)) : 0u;
-                bins[u] = (p < s1 && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1;
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u * kThreads + tid;
+            v[u] = p < s1 ? __ldg(gx + p) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u * kThreads + tid;
+            if (p < s1) {
+                const uint32_t key = order_key(v[u]);
+                if (cached) sk[p - s0] = key;
+                kmax = max(kmax, key);
+                atomicAdd(&hist[key >> 24], 1u);
             }
+        }
+    }
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane == 0) wmax[warp] = kmax;
+    const SliceKeys x{gx, sk, s0, cached};
+
+    // ------------------------------------------------ 1. radix select
+    uint32_t prefix = 0, mask = 0;
+    int need = K;           // keys still to take from the current bin
+    int box = 0;
+    int shift = 24;
+    bool sort_all = false;  // the keys at or above the bin's lower edge are few enough
+    int bin_count = 0;
+    for (;;) {
+        if (shift != 24) {
+            // four positions per thread per step, loaded before any is counted
+            for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
+                int bins[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (bins[u] >= 0) atomicAdd(&hist[buf][bins[u]], 1u);
+                for (int u = 0; u < 4; ++u) {
+                    const int p = p0 + u * kThreads + tid;
+                    const uint32_t key = p < s1 ? x(p) : 0u;
+                    bins[u] = (p < s1 && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (bins[u] >= 0) atomicAdd(&hist[bins[u]], 1u);
+            }
         }
         __syncthreads();
+        push_hist(hist, box0 + box * kSlices * kBins * 4, rank);
+        if (shift == 24 && tid < kSlices) {
+            uint32_t m = 0u;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) m = max(m, wmax[w]);
+            st_cluster_u32(remote_addr(smem_addr(&max_in[rank]), (uint32_t)tid), m);
+        }
         cluster_sync();
         {
-            // the slices' histograms summed in this CTA: thread t adds bins
-            // 8(t%32) .. 8(t%32)+7 of slice t/32 (two 16-byte remote loads per
-            // thread rather than many per thread, as remote loads of one
-            // thread complete one after another)
-            const int r = tid >> 5, b8 = (tid & 31) * 8;
-            const uint32_t src = remote_addr(&hist[buf][b8], (uint32_t)r);
-            const uint4 lo = ld_cluster_v4(src), hi = ld_cluster_v4(src + 16);
-            atomicAdd(&merged[b8 + 0], lo.x); atomicAdd(&merged[b8 + 1], lo.y);
-            atomicAdd(&merged[b8 + 2], lo.z); atomicAdd(&merged[b8 + 3], lo.w);
-            atomicAdd(&merged[b8 + 4], hi.x); atomicAdd(&merged[b8 + 5], hi.y);
-            atomicAdd(&merged[b8 + 6], hi.z); atomicAdd(&merged[b8 + 7], hi.w);
+            uint32_t m = 0;
+#pragma unroll
+            for (int r = 0; r < kSlices; ++r) m += inbox[box][r][tid];
+            abv[tid] = (int)m;
+            if (shift == 24) h1[tid] = (int)m;
+            hist[tid] = 0u;
         }
         __syncthreads();
         if (warp == 0) {
-            // lane l sums bins 255-8l .. 248-8l over the slices (descending);
-            // the first lane whose inclusive count reaches `need` holds the
-            // bin of the K-th largest
+            // lane l sums bins 255-8l .. 248-8l (descending); the first lane
+            // whose inclusive count reaches `need` holds the bin of the K-th
+            // largest
             unsigned c[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) c[j] = merged[255 - (lane * 8 + j)];
+            for (int j = 0; j < 8; ++j) c[j] = (unsigned)abv[255 - (lane * 8 + j)];
             unsigned s = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) s += c[j];
@@ -240,239 +312,200 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
             const unsigned hit = __ballot_sync(0xffffffffu, incl >= (unsigned)need);
             if (lane == __ffs(hit) - 1) {
                 unsigned cum = incl - s;
-                int bin = 255 - lane * 8;
+                int bin = 255 - lane * 8, cnt = (int)c[0];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (cum + c[j] >= (unsigned)need) {
                         bin = 255 - (lane * 8 + j);
+                        cnt = (int)c[j];
                         break;
                     }
                     cum += c[j];
                 }
                 sel[0] = bin;
-                sel[1] = (int)cum;       // candidates above this bin
+                sel[1] = (int)cum;       // keys above this bin
+                sel[2] = cnt;            // keys in it
             }
         }
         __syncthreads();
         need -= sel[1];
         prefix |= (uint32_t)sel[0] << shift;
         mask |= 255u << shift;
-    }
-    // T = prefix; the K-th largest key; `need` keys equal to T are taken
-
-    // ---------------------------------------------------------------- 2. this CTA's candidates
-    int n_above = 0, n_equal = 0;
-    if (K > 0) {
-        for (int p = s0 + tid; p < s1; p += kThreads) {
-            const uint32_t key = order_key(x(p));
-            n_above += key > prefix;
-            n_equal += key == prefix;
+        box ^= 1;
+        bin_count = sel[2];
+        if (K - need + bin_count <= cap) {
+            sort_all = true;
+            break;
         }
+        if (shift == 0) break;           // T = prefix exactly
+        shift -= 8;
     }
-    int tot_above, tot_equal;
-    (void)block_exclusive_scan(n_above, scan_buf, tot_above);
-    (void)block_exclusive_scan(n_equal, scan_buf, tot_equal);
-    if (tid == 0) {
-        counts[0] = tot_above;
-        counts[1] = tot_equal;
-    }
-    __syncthreads();
-    cluster_sync();
-    // the slices before this one: their keys above T and equal to T
-    if (tid < 2 * kSlices)
-        slice_counts[tid / kSlices][tid % kSlices] =
-            (int)ld_cluster_u32(remote_addr(&counts[tid / kSlices], (uint32_t)(tid % kSlices)));
-    __syncthreads();
-    int above_before = 0, equal_before = 0;
+    // The keys to sort: key >= lo.  With sort_all lo is the bin's lower
+    // edge (its low bits are zero); else the keys above T = prefix, and the
+    // first `need` keys equal to T are placed by position.
+    const uint32_t T = prefix;
+    const bool any = sort_all || T != 0xFFFFFFFFu;
+    const uint32_t lo = sort_all ? T : T + 1u;
+
+    // ------------------------------------------------ 2. bins, exchange, scatter
+    {
+        // thread tid takes digit tid: its keys to sort, c (digits above lo's
+        // from the first pass, lo's digit the rest), its share of the bins
+        const int cand = sort_all ? K - need + bin_count : K - need;
+        const int dlo = any ? (int)(lo >> 24) : kBins;
+        int c = tid > dlo ? h1[tid] : 0, above_dlo;
+        (void)block_exclusive_scan(c, scan_buf, above_dlo);
+        if (tid == dlo) c = cand - above_dlo;
+        const int nz = __syncthreads_count(c > 0);
+        int used = 0, width = 0;
+        uint32_t base = 0u;
+        if (c > 0) {
+            uint32_t top = 0u;
 #pragma unroll
-    for (int r = 0; r < kSlices; ++r) {
-        if (r < (int)rank) {
-            above_before += slice_counts[0][r];
-            equal_before += slice_counts[1][r];
+            for (int r = 0; r < kSlices; ++r) top = max(top, max_in[r]);
+            top = min(top, ((uint32_t)tid << 24) | 0xFFFFFFu);
+            base = max(lo, (uint32_t)tid << 24);
+            const long long share = max(1LL, (long long)c * (kBins - nz) / cand);
+            const unsigned long long last = (unsigned long long)(top - base);   // span - 1
+            while ((long long)(last >> width) >= share) ++width;
+            used = (int)(last >> width) + 1;
         }
-    }
-    // keys equal to T taken by this slice: the first take_e of its own
-    const int take_e = K > 0 ? max(0, min(tot_equal, need - equal_before)) : 0;
-    const int m = K > 0 ? tot_above + take_e : 0;          // this CTA's candidates
-    // its list starts after the lists of the slices before it
-    const int taken_before = above_before + min(equal_before, need);
-    if (K > 0 && take_e == tot_equal) {
-        // every key of the slice at or above T is a candidate: any order
-        // (the list is sorted next), slots handed out per warp
-        if (tid == 0) sel[0] = 0;
+        int nbins;
+        const int first = block_exclusive_scan(used, scan_buf, nbins);
+        dbase[tid] = base;
+        dinfo[tid] = first | (width << 16);
         __syncthreads();
-        for (int p0 = s0; p0 < s1; p0 += kThreads) {
-            const int p = p0 + tid;
-            const uint32_t key = p < s1 ? order_key(x(p)) : 0u;
-            const bool c = p < s1 && key >= prefix;
-            const unsigned bal = __ballot_sync(0xffffffffu, c);
-            int base = 0;
-            if (lane == 0 && bal) base = atomicAdd(&sel[0], __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (c) own[base + __popc(bal & ((1u << lane) - 1u))] = pack_cand(key, p);
-        }
-    } else if (K > 0) {
-        // only the first take_e keys equal to T, in position order: thread
-        // tid takes the contiguous positions [q0, q1) and finds where its
-        // keys go from two block-wide scans
-        const int per = (s1 - s0 + kThreads - 1) / kThreads;
-        const int q0 = min(s1, s0 + tid * per), q1 = min(s1, q0 + per);
-        int na = 0, ne = 0;
-        for (int p = q0; p < q1; ++p) {
-            const uint32_t key = order_key(x(p));
-            na += key > prefix;
-            ne += key == prefix;
-        }
-        int ta, te;
-        int ia = block_exclusive_scan(na, scan_buf, ta);
-        int ie = block_exclusive_scan(ne, scan_buf, te);
-        for (int p = q0; p < q1; ++p) {
-            const uint32_t key = order_key(x(p));
-            if (key > prefix) own[ia++] = pack_cand(key, p);
-            else if (key == prefix) {
-                if (ie < take_e) own[tot_above + ie] = pack_cand(key, p);
-                ++ie;
-            }
-        }
     }
-    // pad to a power of two with 0 (sorts last)
-    int P = 1;
-    while (P < m) P <<= 1;
-    for (int i = m + tid; i < P; i += kThreads) own[i] = 0ull;
+    int n_eq = 0;
+    for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
+        int bins[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int p = p0 + u * kThreads + tid;
+            const uint32_t key = p < s1 ? x(p) : 0u;
+            bins[u] = (p < s1 && any && key >= lo) ? key_bin(key, dbase, dinfo) : -1;
+            n_eq += (p < s1 && !sort_all && key == T) ? 1 : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (bins[u] >= 0) atomicAdd(&hist[bins[u]], 1u);
+    }
+    int eq_me = 0;
+    if (!sort_all) (void)block_exclusive_scan(n_eq, scan_buf, eq_me);
     __syncthreads();
+    push_hist(hist, box0 + box * kSlices * kBins * 4, rank);
+    if (!sort_all && tid < kSlices)
+        st_cluster_u32(remote_addr(smem_addr(&eq_in[rank]), (uint32_t)tid), (uint32_t)eq_me);
+    cluster_sync();
 
-    // ---------------------------------------------------------------- 3. sort, rank, place
-    if (P <= kThreads) {
-        // one entry per thread (threads past P hold 0): the same network, the
-        // partner within the warp reached by a shuffle, beyond it through
-        // shared memory
-        unsigned long long v = tid < P ? own[tid] : 0ull;
-        for (int size = 2; size <= kThreads; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                unsigned long long o;
-                if (stride >= 32) {
-                    __syncthreads();
-                    own[tid] = v;
-                    __syncthreads();
-                    o = own[tid ^ stride];
-                } else {
-                    o = __shfl_xor_sync(0xffffffffu, v, stride);
-                }
-                // the lower index of a pair keeps the larger value in a
-                // descending block, the smaller in an ascending one
-                const bool desc = (tid & size) == 0;
-                const bool lower = (tid & stride) == 0;
-                v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-            }
+    // thread tid takes bin kBins-1-tid, so that a block scan runs over the
+    // bins in descending order
+    int total, target;
+    {
+        const int bn = kBins - 1 - tid;
+        int m = 0, before_me = 0;
+#pragma unroll
+        for (int r = 0; r < kSlices; ++r) {
+            const int c = (int)inbox[box][r][bn];
+            m += c;
+            before_me += r < (int)rank ? c : 0;
+        }
+        const int above = block_exclusive_scan(m, scan_buf, total);
+        target = (total + kSlices - 1) / kSlices;
+        const int owner = target ? min(kSlices - 1, above / target) : 0;
+        abv[bn] = above;
+        base_me[bn] = above - owner * target + before_me;
+        hist[bn] = 0u;
+        if (tid == 0) {
+            span[0] = cap;               // no entries: an empty range
+            span[1] = 0;
         }
         __syncthreads();
-        if (tid < P) own[tid] = v;
-        __syncthreads();
-    } else {
-        for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = tid; i < P / 2; i += kThreads) {
-                    const int lo = 2 * i - (i & (stride - 1));
-                    const int hi = lo + stride;
-                    const bool desc = (lo & size) == 0;
-                    const unsigned long long u = own[lo], w = own[hi];
-                    if ((u < w) == desc) {
-                        own[lo] = w;
-                        own[hi] = u;
+        if (m > 0 && owner == (int)rank) {
+            atomicMin(&span[0], above - owner * target);
+            atomicMax(&span[1], above - owner * target + m);
+        }
+    }
+    const uint32_t recv0 = smem_addr(recv);
+    if (any) {
+        for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                if (p < s1) {
+                    const uint32_t key = x(p);
+                    if (key >= lo) {
+                        const int bn = key_bin(key, dbase, dinfo);
+                        const int slot = (int)atomicAdd(&hist[bn], 1u);
+                        const int owner = min(kSlices - 1, abv[bn] / target);
+                        st_cluster_u64(remote_addr(recv0 + 8u * (uint32_t)(base_me[bn] + slot),
+                                                   (uint32_t)owner),
+                                       pack_cand(key, p));
                     }
                 }
-                __syncthreads();
             }
         }
     }
-    if (tid == 0) {
-        counts[2] = taken_before;
-        counts[3] = m;
+    if (!sort_all) {
+        // the first `need` keys equal to T, in position order over the
+        // slices, take places K-need .. K-1: thread tid walks the contiguous
+        // positions [q0, q1) and finds its keys' places from a block scan
+        int eq_before = 0;
+#pragma unroll
+        for (int r = 0; r < kSlices; ++r) eq_before += r < (int)rank ? (int)eq_in[r] : 0;
+        const int take = max(0, min(eq_me, need - eq_before));
+        if (take > 0) {
+            const int per = (s1 - s0 + kThreads - 1) / kThreads;
+            const int q0 = min(s1, s0 + tid * per), q1 = min(s1, q0 + per);
+            int ne = 0;
+            for (int p = q0; p < q1; ++p) ne += x(p) == T ? 1 : 0;
+            int te;
+            int ie = block_exclusive_scan(ne, scan_buf, te);
+            for (int p = q0; p < q1 && ie < take; ++p) {
+                if (x(p) == T) {
+                    const int rk = K - need + eq_before + ie;
+                    oi[rk] = p;
+                    if (ov) ov[rk] = key_bits(T);
+                    ++ie;
+                }
+            }
+        }
     }
-    __syncthreads();
     cluster_sync();
-    // every list into `all`, each at its offset (this CTA's own too)
-    if (tid < 2 * kSlices)
-        slice_counts[2 + tid / kSlices][tid % kSlices] =
-            (int)ld_cluster_u32(remote_addr(&counts[2 + tid / kSlices], (uint32_t)(tid % kSlices)));
-    __syncthreads();
-    int offs[kSlices], lens[kSlices];
-#pragma unroll
-    for (int r = 0; r < kSlices; ++r) {
-        offs[r] = slice_counts[2][r];
-        lens[r] = slice_counts[3][r];
-    }
-    // entry j of the concatenated lists (list r holds [offs[r], offs[r] +
-    // lens[r])), eight loads in flight per thread
-    for (int j0 = 0; j0 < K; j0 += 8 * kThreads) {
-        unsigned long long v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = j0 + u * kThreads + tid;
-            v[u] = 0ull;
-            if (j < K) {
-                int r = 0;
-#pragma unroll
-                for (int q = 1; q < kSlices; ++q) r += j >= offs[q] ? 1 : 0;
-                v[u] = ld_cluster_u64(remote_addr(own + (j - offs[r]), (uint32_t)r));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = j0 + u * kThreads + tid;
-            if (j < K) all[j] = v[u];
+
+    // ------------------------------------------------ 3. rank the received entries
+    for (int i = span[0] + tid; i < span[1]; i += kThreads) {
+        const unsigned long long e = recv[i];
+        const uint32_t key = (uint32_t)(e >> 32);
+        const int bn = key_bin(key, dbase, dinfo);
+        const int first = abv[bn] - (int)rank * target;
+        const int n = (bn == 0 ? total : abv[bn - 1]) - abv[bn];
+        int before = 0;
+        for (int j = first; j < first + n; ++j) before += recv[j] > e ? 1 : 0;
+        const int rk = abv[bn] + before;
+        if (rk < K) {
+            oi[rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)e);
+            if (ov) ov[rk] = key_bits(key);
         }
     }
-    __syncthreads();
-    int32_t* oi = a.indices + (long long)row * a.indices_stride;
-    uint32_t* ov = a.values ? reinterpret_cast<uint32_t*>(a.values) + (long long)row * a.values_stride
-                            : nullptr;
-    for (int i = tid; i < m; i += kThreads) {
-        const unsigned long long c = own[i];
-        int rk = i;
-        for (int r = 0; r < kSlices; ++r) {
-            if (r == (int)rank) continue;
-            // entries of list r greater than c (the list is descending)
-            int lo = 0, hi = lens[r];
-            const unsigned long long* L = all + offs[r];
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (L[mid] > c) lo = mid + 1;
-                else hi = mid;
-            }
-            rk += lo;
-        }
-        oi[rk] = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
-        if (ov) ov[rk] = key_bits((uint32_t)(c >> 32));
-    }
-    if (rank == 0) {
-        for (int i = K + tid; i < a.k; i += kThreads) {
-            oi[i] = -1;
-            if (ov) ov[i] = 0xFF800000u;     // -inf
-        }
-    }
-    // no CTA leaves while another may still read its shared memory
-    cluster_sync();
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_t stream)
 {
-    // dynamic shared memory: the sort buffer (k rounded up to a power of
-    // two, at least kThreads), the lists of all slices (k), and the largest slice copy that fits
-    // under a budget that keeps four CTAs on an SM (larger slices are read
-    // from global memory on every pass)
-    // (at least one entry per thread: the in-register sort goes through it)
-    int sort_cap = kThreads;
-    while (sort_cap < a.k) sort_cap <<= 1;
-    const size_t lists = (size_t)(sort_cap + a.k) * 8;
-    const size_t budget = 54 * 1024;
+    // dynamic shared memory: the received entries (k + kCapExtra) and the
+    // largest slice copy that fits under a budget that keeps four CTAs on an
+    // SM (k <= 2048; beyond, enough for a 32768-position row's slice) --
+    // larger slices are read from global memory on every pass
+    const int cap = a.k + kCapExtra;
+    const size_t entries = (size_t)cap * 8;
+    const size_t budget = entries <= 20 * 1024 ? 36 * 1024 : entries + 16 * 1024;
     const long long chunk = ((long long)a.max_context + kSlices - 1) / kSlices;
-    long long cache_elems = budget > lists ? (long long)(budget - lists) / 4 : 0;
+    long long cache_elems = (long long)(budget - entries) / 4;
     if (cache_elems > chunk) cache_elems = chunk;
-    const size_t smem = lists + (size_t)cache_elems * 4;
-    if (smem + 4 * 1024 > (size_t)smem_optin) return cudaErrorInvalidConfiguration;
+    const size_t smem = entries + (size_t)cache_elems * 4;
+    if (smem + 24 * 1024 > (size_t)smem_optin) return cudaErrorInvalidConfiguration;
     static int configured_device = -1;
     static size_t configured_bytes = 0;
     int dev = 0;
@@ -496,7 +529,7 @@ cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel, a, (int)cache_elems, sort_cap);
+    e = cudaLaunchKernelEx(&cfg, topk_kernel, a, (int)cache_elems, cap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
