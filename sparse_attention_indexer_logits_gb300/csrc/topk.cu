@@ -55,6 +55,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;          // radix digits; bins of the keys to sort
 constexpr int kCapExtra = 256;      // keys past K a row may take into the sort
+constexpr int kPer = 16;            // keys a thread holds in registers
+constexpr int kRegKeys = kPer * kThreads;   // the largest slice held in registers
 
 // Keys and values stay integer bit patterns throughout: a float register can
 // be canonicalised on its way (a NaN payload or sign lost), and the order
@@ -142,6 +144,37 @@ struct SliceKeys {
     }
 };
 
+// Calls f(key, p) for every key of the slice [s0, s1): from the registers
+// (key u of thread t at position s0 + u*kThreads + t) when the slice fits
+// them, else from `x`, kPer keys per thread loaded before any is visited.
+template <bool kRegs, typename F>
+__device__ __forceinline__ void visit_keys(const uint32_t (&reg)[kPer], const SliceKeys& x, int s0,
+                                           int s1, F&& f)
+{
+    const int tid = threadIdx.x;
+    if constexpr (kRegs) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int p = s0 + u * kThreads + tid;
+            if (p < s1) f(reg[u], p);
+        }
+    } else {
+        for (int p0 = s0; p0 < s1; p0 += kRegKeys) {
+            uint32_t v[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                v[u] = p < s1 ? x(p) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                if (p < s1) f(v[u], p);
+            }
+        }
+    }
+}
+
 // Block-wide exclusive scan of one int per thread (kThreads threads); also
 // returns the total.  Uses `buf` (kWarps ints).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* buf, int& total)
@@ -179,13 +212,16 @@ __device__ __forceinline__ void push_hist(const uint32_t* hist, uint32_t box, ui
     st_cluster_v4(remote_addr(local, (uint32_t)c0 + 1), v);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int cache_elems, int cap)
+// kRegs: the slice (at most kRegKeys keys) is held in registers; else in
+// shared memory when it fits (cache_elems), or read from global memory.
+template <bool kRegs>
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, int cache_elems, int cap)
 {
     __shared__ __align__(16) uint32_t inbox[2][kSlices][kBins];   // the slices' histograms
     __shared__ __align__(16) uint32_t hist[kBins];   // this CTA's histogram, then the bins' slot counters
     __shared__ int abv[kBins];        // summed histogram (radix passes); keys in higher bins (sort)
-    __shared__ int base_me[kBins];    // where this CTA's keys of a bin go in the owner's entries
-    int* const h1 = base_me;          // before it: the row's first-pass histogram
+    __shared__ int dest[kBins];       // a bin's owner << 24 | where this CTA's keys of it go there
+    int* const h1 = dest;             // before it: the row's first-pass histogram
     __shared__ uint32_t dbase[kBins];  // per digit: lowest key of its bins
     __shared__ int dinfo[kBins];       // per digit: first bin | bin width bits << 16
     __shared__ uint32_t eq_in[kSlices];   // the slices' counts of keys equal to T
@@ -223,28 +259,47 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
     const int s0 = min(lim, (int)rank * chunk), s1 = min(lim, s0 + chunk);
     const uint32_t* gx =
         reinterpret_cast<const uint32_t*>(a.logits) + (long long)row * a.logits_stride;
-    const bool cached = chunk <= cache_elems;
+    const bool cached = !kRegs && chunk <= cache_elems;
     const uint32_t box0 = smem_addr(&inbox[0][0][0]);
 
     // ------------------------------------------------ the slice's keys and the first histogram
     hist[tid] = 0u;
     __syncthreads();
     uint32_t kmax = 0u;
-    for (int p0 = s0; p0 < s1; p0 += 8 * kThreads) {
-        uint32_t v[8];
+    uint32_t reg[kPer];
+    if constexpr (kRegs) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int p = p0 + u * kThreads + tid;
-            v[u] = p < s1 ? __ldg(gx + p) : 0u;
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int u = h * 8; u < h * 8 + 8; ++u) {
+                const int p = s0 + u * kThreads + tid;
+                reg[u] = p < s1 ? order_key(__ldg(gx + p)) : 0u;
+            }
+#pragma unroll
+            for (int u = h * 8; u < h * 8 + 8; ++u) {
+                if (s0 + u * kThreads + tid < s1) {
+                    kmax = max(kmax, reg[u]);
+                    atomicAdd(&hist[reg[u] >> 24], 1u);
+                }
+            }
         }
+    } else {
+        for (int p0 = s0; p0 < s1; p0 += 8 * kThreads) {
+            uint32_t v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int p = p0 + u * kThreads + tid;
-            if (p < s1) {
-                const uint32_t key = order_key(v[u]);
-                if (cached) sk[p - s0] = key;
-                kmax = max(kmax, key);
-                atomicAdd(&hist[key >> 24], 1u);
+            for (int u = 0; u < 8; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                v[u] = p < s1 ? __ldg(gx + p) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int p = p0 + u * kThreads + tid;
+                if (p < s1) {
+                    const uint32_t key = order_key(v[u]);
+                    if (cached) sk[p - s0] = key;
+                    kmax = max(kmax, key);
+                    atomicAdd(&hist[key >> 24], 1u);
+                }
             }
         }
     }
@@ -261,19 +316,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
     int bin_count = 0;
     for (;;) {
         if (shift != 24) {
-            // four positions per thread per step, loaded before any is counted
-            for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
-                int bins[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int p = p0 + u * kThreads + tid;
-                    const uint32_t key = p < s1 ? x(p) : 0u;
-                    bins[u] = (p < s1 && (key & mask) == prefix) ? (int)((key >> shift) & 255u) : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (bins[u] >= 0) atomicAdd(&hist[bins[u]], 1u);
-            }
+            visit_keys<kRegs>(reg, x, s0, s1, [&](uint32_t key, int) {
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            });
         }
         __syncthreads();
         push_hist(hist, box0 + box * kSlices * kBins * 4, rank);
@@ -365,9 +410,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
             for (int r = 0; r < kSlices; ++r) top = max(top, max_in[r]);
             top = min(top, ((uint32_t)tid << 24) | 0xFFFFFFu);
             base = max(lo, (uint32_t)tid << 24);
+            // at most `share` bins of width 2^width: the least width with
+            // (span - 1) >> width < share
             const long long share = max(1LL, (long long)c * (kBins - nz) / cand);
             const unsigned long long last = (unsigned long long)(top - base);   // span - 1
-            while ((long long)(last >> width) >= share) ++width;
+            if ((long long)last >= share) {
+                width = (64 - __clzll((long long)last)) - (64 - __clzll(share));
+                width += (long long)(last >> width) >= share ? 1 : 0;
+            }
             used = (int)(last >> width) + 1;
         }
         int nbins;
@@ -377,19 +427,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
         __syncthreads();
     }
     int n_eq = 0;
-    for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
-        int bins[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int p = p0 + u * kThreads + tid;
-            const uint32_t key = p < s1 ? x(p) : 0u;
-            bins[u] = (p < s1 && any && key >= lo) ? key_bin(key, dbase, dinfo) : -1;
-            n_eq += (p < s1 && !sort_all && key == T) ? 1 : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (bins[u] >= 0) atomicAdd(&hist[bins[u]], 1u);
-    }
+    visit_keys<kRegs>(reg, x, s0, s1, [&](uint32_t key, int) {
+        if (any && key >= lo) atomicAdd(&hist[key_bin(key, dbase, dinfo)], 1u);
+        n_eq += key == T ? 1 : 0;
+    });
     int eq_me = 0;
     if (!sort_all) (void)block_exclusive_scan(n_eq, scan_buf, eq_me);
     __syncthreads();
@@ -414,7 +455,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
         target = (total + kSlices - 1) / kSlices;
         const int owner = target ? min(kSlices - 1, above / target) : 0;
         abv[bn] = above;
-        base_me[bn] = above - owner * target + before_me;
+        dest[bn] = (owner << 24) | (above - owner * target + before_me);
         hist[bn] = 0u;
         if (tid == 0) {
             span[0] = cap;               // no entries: an empty range
@@ -428,28 +469,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a, int ca
     }
     const uint32_t recv0 = smem_addr(recv);
     if (any) {
-        for (int p0 = s0; p0 < s1; p0 += 4 * kThreads) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int p = p0 + u * kThreads + tid;
-                if (p < s1) {
-                    const uint32_t key = x(p);
-                    if (key >= lo) {
-                        const int bn = key_bin(key, dbase, dinfo);
-                        const int slot = (int)atomicAdd(&hist[bn], 1u);
-                        const int owner = min(kSlices - 1, abv[bn] / target);
-                        st_cluster_u64(remote_addr(recv0 + 8u * (uint32_t)(base_me[bn] + slot),
-                                                   (uint32_t)owner),
-                                       pack_cand(key, p));
-                    }
-                }
+        visit_keys<kRegs>(reg, x, s0, s1, [&](uint32_t key, int p) {
+            if (key >= lo) {
+                const int bn = key_bin(key, dbase, dinfo);
+                const int slot = (int)atomicAdd(&hist[bn], 1u);
+                const int d = dest[bn];
+                st_cluster_u64(remote_addr(recv0 + 8u * (uint32_t)((d & 0xFFFFFF) + slot), (uint32_t)(d >> 24)),
+                               pack_cand(key, p));
             }
-        }
+        });
     }
     if (!sort_all) {
         // the first `need` keys equal to T, in position order over the
         // slices, take places K-need .. K-1: thread tid walks the contiguous
-        // positions [q0, q1) and finds its keys' places from a block scan
+        // positions [q0, q1) (read through `x`: from global memory when the
+        // slice is in registers) and finds its keys' places from a block scan
         int eq_before = 0;
 #pragma unroll
         for (int r = 0; r < kSlices; ++r) eq_before += r < (int)rank ? (int)eq_in[r] : 0;
@@ -500,22 +534,27 @@ cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_
     // larger slices are read from global memory on every pass
     const int cap = a.k + kCapExtra;
     const size_t entries = (size_t)cap * 8;
-    const size_t budget = entries <= 20 * 1024 ? 36 * 1024 : entries + 16 * 1024;
     const long long chunk = ((long long)a.max_context + kSlices - 1) / kSlices;
-    long long cache_elems = (long long)(budget - entries) / 4;
-    if (cache_elems > chunk) cache_elems = chunk;
+    const bool regs = chunk <= kRegKeys;
+    long long cache_elems = 0;
+    if (!regs) {
+        const size_t budget = entries <= 20 * 1024 ? 36 * 1024 : entries + 16 * 1024;
+        cache_elems = (long long)(budget - entries) / 4;
+        if (cache_elems > chunk) cache_elems = chunk;
+    }
     const size_t smem = entries + (size_t)cache_elems * 4;
     if (smem + 24 * 1024 > (size_t)smem_optin) return cudaErrorInvalidConfiguration;
-    static int configured_device = -1;
-    static size_t configured_bytes = 0;
+    void (*kernel)(const TopkArgs, int, int) = regs ? topk_kernel<true> : topk_kernel<false>;
+    static int configured_device[2] = {-1, -1};
+    static size_t configured_bytes[2] = {0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev || configured_bytes < smem) {
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (configured_device[regs] != dev || configured_bytes[regs] < smem) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
-        configured_bytes = smem;
+        configured_device[regs] = dev;
+        configured_bytes[regs] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows * kSlices);
@@ -529,7 +568,7 @@ cudaError_t launch_topk(const TopkArgs& a, int rows, int smem_optin, cudaStream_
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel, a, (int)cache_elems, cap);
+    e = cudaLaunchKernelEx(&cfg, kernel, a, (int)cache_elems, cap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
