@@ -467,11 +467,13 @@ def indexer_nvfp4(group_size: int, seed: int = 6, groups: int = 256, max_context
 
 def topk_logits_input(batch: int, next_n: int, max_context: int, seed: int = 9,
                       lo: int = 0, hi: int | None = None, distinct: int | None = None,
-                      specials: bool = True):
+                      specials: bool = True, narrow: bool = False):
     """Synthetic logits rows [batch*next_n, max_context] and seq_lens for the
     top-k selection: values ~N(0, 4) (or ``distinct`` levels only, for many
-    ties), seq_lens uniform on [lo, hi] (default [0, max_context]); with
-    ``specials`` some rows carry +-inf, signed zeros and a NaN."""
+    ties; or, ``narrow``, 1 + j * 2^-23 for j uniform below 2^15: values that
+    agree in their top 16 bits), seq_lens uniform on [lo, hi] (default [0,
+    max_context]); with ``specials`` some rows carry +-inf, signed zeros and a
+    NaN."""
     g = rng(seed)
     hi = max_context if hi is None else hi
     seq_lens = g.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
@@ -479,6 +481,9 @@ def topk_logits_input(batch: int, next_n: int, max_context: int, seed: int = 9,
     if distinct:
         x = g.integers(-distinct // 2, distinct - distinct // 2, size=(rows, max_context))
         x = x.astype(np.float32)
+    elif narrow:
+        j = g.integers(0, 1 << 15, size=(rows, max_context)).astype(np.uint32)
+        x = (np.uint32(0x3F800000) + j).view(np.float32)
     else:
         x = (g.standard_normal((rows, max_context), dtype=np.float32) * 4).astype(np.float32)
     if specials and rows > 0 and max_context >= 8:

@@ -2,8 +2,12 @@
 and selected values): k from 1 to 4096, ties (few distinct values), rows
 with fewer candidates than k, empty requests, next_n 1..4, special values
 (+-inf, signed zeros, NaN), max_context clipping, and a decode-sized batch
-(64 rows x 32768, k = 2048).  The inputs are synthetic logits from the
-seeded generator, not outputs of the logits kernel."""
+(64 rows x 32768, k = 2048).  Further cases steer the kernel down each of
+its paths: the radix select stopping after the first, second or third pass,
+the exact threshold with the tied keys placed by position, and slices too
+long for registers (from shared memory, and from global memory).  The
+inputs are synthetic logits from the seeded generator, not outputs of the
+logits kernel."""
 import numpy as np
 import pytest
 import torch
@@ -63,3 +67,30 @@ def test_indices_only():
     gi, _ = run(x, sl, 1, 1000, 50, with_values=False)
     ri, _ = oracle.topk_logits(x, sl, 1, 1000, 50)
     assert np.array_equal(gi, ri)
+
+
+def test_exact_threshold_with_ties_placed_by_position():
+    # three levels, k = 1500 of 3000-4000: the keys equal to the threshold
+    # outnumber k + 256, so the select runs all four passes; the keys above
+    # it go through the bins, the tied ones take the last places by position
+    x, sl = W.topk_logits_input(4, 2, 4000, seed=521, distinct=3, lo=3000)
+    check(x, sl, 2, 4000, 1500)
+
+
+def test_select_stops_after_the_third_pass():
+    # values that agree in their top 16 bits: the second pass cannot narrow
+    # the candidates, the third can
+    x, sl = W.topk_logits_input(4, 1, 4000, seed=522, lo=3000, narrow=True, specials=False)
+    check(x, sl, 1, 4000, 300)
+
+
+def test_long_rows_sliced_into_shared_memory():
+    # 36000 positions: slices of 4500 keys, beyond the registers' 4096
+    x, sl = W.topk_logits_input(4, 1, 36000, seed=523, lo=33000)
+    check(x, sl, 1, 36000, 2048)
+
+
+def test_long_rows_read_from_global_memory():
+    # 70000 positions: slices of 8750 keys, beyond the shared-memory copy
+    x, sl = W.topk_logits_input(3, 1, 70000, seed=524, lo=60000)
+    check(x, sl, 1, 70000, 1024)
