@@ -43,11 +43,11 @@
 // A tile is 2H 64-key blocks (H = 2 halves of M = 128 at one query slot per
 // pass, H = 1 at two): the codes land by TMA with the 64-byte swizzle (a
 // 64-byte row is one swizzle span), two blocks of a half being the MMA's
-// K-major operand as they land; the 256 scale bytes of a block by cp.async.
+// K-major operand as they land; the 256 scale bytes of a block by a bulk copy.
 //
 //   warps 0,2,3 producers, tile i to warp i % 3: block-table entries from a
-//               64-entry window, per block a TMA of the codes and 16-byte
-//               cp.async of the scales onto the stage's barrier; for the
+//               64-entry window, per block a TMA of the codes and a bulk
+//               copy of its scales onto the stage's barrier; for the
 //               owner of a request's first tile also the request's query rows
 //               (TMA, 64-byte swizzle), raw scales and weights (bulk copies)
 //               into a Q slot.  One warp's round takes about twice a tile's
@@ -267,13 +267,6 @@ __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& x, uint32_t& 
                  : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
@@ -370,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sched[0] = sb; sched[1] = sj; sched[2] = eb; sched[3] = ej;
             *abort_flag = 0;
             for (int s = 0; s < S; ++s) {
-                mbar_init(full_bar(s), 1 + 32);   // expect_tx arrival + each lane's cp.async
+                mbar_init(full_bar(s), 1);
                 mbar_init(sfree_bar(s), 1);
             }
             for (int i = 0; i < kSfaSlots; ++i) {
@@ -488,22 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 const uint32_t dst = stage0 + (uint32_t)s * P::kStageBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * kBlockCodeBytes);
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nload * (kBlockCodeBytes + kBlockScaleBytes));
 #pragma unroll
                     for (int cc = 0; cc < TB; ++cc)
-                        if (cc < nload)
+                        if (cc < nload) {
                             tma_load_3d_stream(dst + cc * kBlockCodeBytes, &kmap, full_bar(s), 0, 0,
                                                page[cc], policy);
+                            bulk_load_stream(dst + P::kStageCodes + cc * kBlockScaleBytes,
+                                             a.kv + (long long)page[cc] * kMxfp4BlockBytes + kBlockCodeBytes,
+                                             kBlockScaleBytes, full_bar(s), policy);
+                        }
                 }
-                if (lane < kBlockScaleBytes / 16) {
-#pragma unroll
-                    for (int cc = 0; cc < TB; ++cc)
-                        if (cc < nload)
-                            cp_async16(dst + P::kStageCodes + cc * kBlockScaleBytes + 16u * lane,
-                                       a.kv + (long long)page[cc] * kMxfp4BlockBytes +
-                                           kBlockCodeBytes + 16 * lane);
-                }
-                cp_async_arrive(full_bar(s));
             }
             w.advance(c);
             ++it;
@@ -513,7 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every copy this warp issued lands before the CTA may exit: of its
         // stages only the last S tiles' can be in flight, of its query loads
         // only those of the last two requests
-        cp_async_wait_all();
         if (lane == 0) {
             for (int t = (it > S ? it - S : 0); t < it; ++t)
                 if (t % kProducers == prod) mbar_wait_drain(full_bar(t % S), (uint32_t)(t / S) & 1u);
