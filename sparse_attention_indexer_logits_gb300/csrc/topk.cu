@@ -11,7 +11,9 @@
 //
 // A row is one cluster of kSlices CTAs; CTA s of the cluster holds the
 // slice [s*chunk, min(lim, (s+1)*chunk)) of the row, chunk = ceil(lim /
-// kSlices), as order keys in shared memory when it fits.  Every exchange
+// kSlices), as order keys: in registers, kPer a thread, when the slice has
+// at most kRegKeys of them; else in shared memory when it fits, or read from
+// global memory on every pass.  Every exchange
 // between the CTAs is a push: a CTA stores into the others' shared memory
 // (distributed shared memory) and one cluster barrier later they read it
 // locally.
